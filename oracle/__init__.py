@@ -1,0 +1,203 @@
+"""CPU oracle for MXNorm -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product path (the CUDA library and its
+Python binding) never imports, links or runs anything here, and this package
+never imports the product.  The arithmetic lives in ``mxnorm_oracle.c``
+(plain scalar C, fp64); this module only compiles it with gcc and marshals
+numpy arrays.  ``bruteforce.py`` is a second, pure-Python implementation in
+exact rational arithmetic for tiny inputs.
+
+Method sources (by page title and section):
+  * "MXNorm: Reusing MXFP block scales for efficient tensor normalisation",
+    Resumen tecnico, 2. Metodologia, "Fundamentos Teoricos" (formula) and
+    "Implementacion" (fusion of the norm and the MX cast);
+  * the same paper's English abstract (scales reused from the MXFP8 cast);
+  * "Entrenamiento Previo ... con MXFP4", Metodologia, item 3 (deterministic
+    H16 Hadamard rotation);
+  * OCP Microscaling Formats v1.0, sections 5 and 6.3 (encodings, shared
+    exponent rule).
+
+Parity status of each function is stated in its docstring; all are pinned by
+the ``-m "not gpu"`` tests except the statistical behaviour of the estimator
+(the pages' Theorem 1), which the pages give no constant for: parity
+unpinned there, and no function here claims it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+FMT_MXFP8_E4M3 = 0
+FMT_MXFP4_E2M1 = 1
+FMT_MXFP4_E2M1_H16 = 2
+FMT_NAMES = {"mxfp8": FMT_MXFP8_E4M3, "mxfp4": FMT_MXFP4_E2M1, "mxfp4_h16": FMT_MXFP4_E2M1_H16}
+BLOCK = 32
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mxnorm_oracle.c")
+_LIB = os.path.join(_HERE, "libmxnorm_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (-O2, no fast-math, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                               "-fno-fast-math", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    i64, i32, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    p = ctypes.c_void_p
+    lib.oracle_mxnorm_rows.argtypes = [p, i64, i64, i32, i32, p, p, p]
+    lib.oracle_mxnorm_rows.restype = i32
+    lib.oracle_mx_cast_rows.argtypes = [p, i64, i64, i32, p, p]
+    lib.oracle_mx_cast_rows.restype = i32
+    lib.oracle_rmsnorm_mxfp8_rows.argtypes = [p, i64, i64, f32, p, p, p, p]
+    lib.oracle_rmsnorm_mxfp8_rows.restype = i32
+    lib.oracle_cast_e4m3_array.argtypes = [p, i64, p]
+    lib.oracle_cast_e2m1_array.argtypes = [p, i64, p]
+    lib.oracle_e8m0_exponent_array.argtypes = [p, i64, i32, p]
+    lib.oracle_h16_groups.argtypes = [p, i64, p]
+    lib.oracle_float_to_bf16_array.argtypes = [p, i64, p]
+    lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
+    lib.oracle_decode_e4m3.restype = ctypes.c_double
+    lib.oracle_decode_e2m1.argtypes = [ctypes.c_uint8]
+    lib.oracle_decode_e2m1.restype = ctypes.c_double
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _fmt_id(fmt) -> int:
+    return FMT_NAMES[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def _as_bf16_bits(x) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.uint16:
+        raise TypeError("oracle inputs are bf16 bit patterns (uint16)")
+    return x
+
+
+def code_bytes_per_row(H: int, fmt) -> int:
+    return H if _fmt_id(fmt) == FMT_MXFP8_E4M3 else H // 2
+
+
+def mxnorm_quant(x_bits: np.ndarray, p: int = 2, fmt="mxfp8"):
+    """MXNorm forward of bf16 rows [T, H]: (codes u8, scales u8 [T, H/32], inv_rms f32 [T]).
+
+    Follows the estimator of "MXNorm ...", Fundamentos Teoricos, with
+    m~_k = s_k (the E8M0 scale) and c(p,B) = 1.  Pinned by the closed-form,
+    exhaustive and brute-force tests under tests/.
+    """
+    lib = _load()
+    x = _as_bf16_bits(x_bits)
+    T, H = x.shape
+    f = _fmt_id(fmt)
+    codes = np.empty((T, code_bytes_per_row(H, f)), np.uint8)
+    scales = np.empty((T, H // BLOCK), np.uint8)
+    inv = np.empty((T,), np.float32)
+    rc = lib.oracle_mxnorm_rows(_ptr(x), T, H, int(p), f, _ptr(codes), _ptr(scales), _ptr(inv))
+    if rc != 0:
+        raise ValueError(f"oracle rejected arguments T={T} H={H} p={p} fmt={fmt}")
+    return codes, scales, inv
+
+
+def mx_cast(x_bits: np.ndarray, fmt="mxfp8"):
+    """MX cast only (codes, scales) of bf16 rows [T, H]; OCP MX v1.0 6.3."""
+    lib = _load()
+    x = _as_bf16_bits(x_bits)
+    T, H = x.shape
+    f = _fmt_id(fmt)
+    codes = np.empty((T, code_bytes_per_row(H, f)), np.uint8)
+    scales = np.empty((T, H // BLOCK), np.uint8)
+    if lib.oracle_mx_cast_rows(_ptr(x), T, H, f, _ptr(codes), _ptr(scales)) != 0:
+        raise ValueError("oracle rejected arguments")
+    return codes, scales
+
+
+def rmsnorm_mxfp8(x_bits: np.ndarray, eps: float = 1e-5):
+    """Two-pass baseline: RMSNorm (no gain) then MXFP8 cast of its bf16 output.
+
+    Returns (y bf16 bits [T, H], codes, scales, inv_rms)."""
+    lib = _load()
+    x = _as_bf16_bits(x_bits)
+    T, H = x.shape
+    y = np.empty((T, H), np.uint16)
+    codes = np.empty((T, H), np.uint8)
+    scales = np.empty((T, H // BLOCK), np.uint8)
+    inv = np.empty((T,), np.float32)
+    if lib.oracle_rmsnorm_mxfp8_rows(_ptr(x), T, H, float(eps), _ptr(y), _ptr(codes), _ptr(scales), _ptr(inv)) != 0:
+        raise ValueError("oracle rejected arguments")
+    return y, codes, scales, inv
+
+
+def cast_e4m3(r) -> np.ndarray:
+    """Saturating RNE E4M3 codes of finite reals r (any shape)."""
+    lib = _load()
+    r = np.ascontiguousarray(r, dtype=np.float64)
+    out = np.empty(r.shape, np.uint8)
+    lib.oracle_cast_e4m3_array(_ptr(r), r.size, _ptr(out))
+    return out
+
+
+def cast_e2m1(r) -> np.ndarray:
+    """Saturating RNE E2M1 nibbles (0..15) of finite reals r (any shape)."""
+    lib = _load()
+    r = np.ascontiguousarray(r, dtype=np.float64)
+    out = np.empty(r.shape, np.uint8)
+    lib.oracle_cast_e2m1_array(_ptr(r), r.size, _ptr(out))
+    return out
+
+
+def e8m0_exponent(amax, emax_elem: int) -> np.ndarray:
+    """Shared exponent clamp(floor(log2 amax) - emax_elem, -127, 127), 0 -> -127."""
+    lib = _load()
+    a = np.ascontiguousarray(amax, dtype=np.float64)
+    out = np.empty(a.shape, np.int32)
+    lib.oracle_e8m0_exponent_array(_ptr(a), a.size, int(emax_elem), _ptr(out))
+    return out
+
+
+def h16(v) -> np.ndarray:
+    """(1/4) * H16 applied to each consecutive group of 16 fp32 values."""
+    lib = _load()
+    a = np.ascontiguousarray(v, dtype=np.float32)
+    if a.size % 16:
+        raise ValueError("h16 needs a multiple of 16 values")
+    out = np.empty_like(a)
+    lib.oracle_h16_groups(_ptr(a), a.size // 16, _ptr(out))
+    return out
+
+
+def float_to_bf16(v) -> np.ndarray:
+    """Round fp32 values to bf16 bit patterns, nearest, ties to even."""
+    lib = _load()
+    a = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(a.shape, np.uint16)
+    lib.oracle_float_to_bf16_array(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def decode_e4m3(code: int) -> float:
+    return _load().oracle_decode_e4m3(int(code))
+
+
+def decode_e2m1(nibble: int) -> float:
+    return _load().oracle_decode_e2m1(int(nibble))

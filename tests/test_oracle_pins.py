@@ -1,0 +1,372 @@
+"""Pins of the CPU oracle against facts fixed outside it.
+
+Every test here checks the oracle (oracle/) against something it does not
+compute itself: the bit-field definitions of bf16/E4M3/E2M1/E8M0 (OCP
+Microscaling Formats v1.0, sections 5 and 6.3), library conversions (torch's
+float8_e4m3fn cast, ml_dtypes' float4_e2m1fn cast), scipy's Sylvester
+Hadamard matrix, closed forms of the estimator of "MXNorm: Reusing MXFP
+block scales for efficient tensor normalisation" (Resumen tecnico, 2.
+Metodologia, Fundamentos Teoricos) on constant and two-level rows, the
+growth bounds of its section 4 ("Analisis de Picos": O(K) for p = 1 against
+RMSNorm's O(sqrt(D))), and an exact-rational brute force on tiny rows.
+No GPU is used.
+"""
+from fractions import Fraction
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from mx_scale_reusing_gb300 import synth
+
+ALL_BF16 = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+
+
+def bf16_values(bits):
+    return synth.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def finite_bf16_bits():
+    b = ALL_BF16
+    return b[((b >> 7) & 0xFF) != 0xFF]
+
+
+# ----------------------------------------------------------------- E8M0
+@pytest.mark.parametrize("emax", [8, 2])
+def test_e8m0_exponent_exhaustive_vs_bit_fields(oracle_mod, emax):
+    """All 32640 finite non-negative bf16 amax values: the oracle's
+    floor(log2) via frexp must equal the exponent read off the bf16 bit
+    fields (normal: E - 127; subnormal: bit_length(M) - 1 - 133)."""
+    bits = finite_bf16_bits()
+    bits = bits[bits < 0x8000]
+    got = oracle_mod.e8m0_exponent(bf16_values(bits), emax)
+    E = (bits.astype(np.int64) >> 7) & 0xFF
+    M = bits.astype(np.int64) & 0x7F
+    fl = np.where(E > 0, E - 127, np.array([int(m).bit_length() - 1 - 133 if m else 0 for m in M]))
+    want = np.clip(fl - emax, -127, 127)
+    want[bits == 0] = -127
+    np.testing.assert_array_equal(got, want)
+
+
+def test_e8m0_exponent_fp32_range(oracle_mod):
+    a = np.array([2.0 ** -149, 2.0 ** -126, 1.0, 1.9999, 2.0, 448.0, 3.0e38])
+    np.testing.assert_array_equal(oracle_mod.e8m0_exponent(a, 8), [-127, -127, -8, -8, -7, 0, 119])
+
+
+# ----------------------------------------------------------------- E4M3
+def test_e4m3_decode_table(oracle_mod):
+    """Spot values of the E4M3 encoding (bias 7, 3 mantissa bits, no Inf)."""
+    assert oracle_mod.decode_e4m3(0x7E) == 448.0
+    assert oracle_mod.decode_e4m3(0x38) == 1.0
+    assert oracle_mod.decode_e4m3(0x08) == 2.0 ** -6
+    assert oracle_mod.decode_e4m3(0x01) == 2.0 ** -9
+    assert oracle_mod.decode_e4m3(0x07) == 7 * 2.0 ** -9
+    assert oracle_mod.decode_e4m3(0xC0) == -2.0
+    assert math.isnan(oracle_mod.decode_e4m3(0x7F)) and math.isnan(oracle_mod.decode_e4m3(0xFF))
+    mags = [oracle_mod.decode_e4m3(c) for c in range(127)]
+    assert all(a < b for a, b in zip(mags, mags[1:]))
+
+
+def test_e4m3_cast_exhaustive_bf16_vs_torch(oracle_mod):
+    """Every finite bf16 value r (the values r = x / 2^e a bf16 x can give):
+    where |r| <= 464 torch's float8_e4m3fn conversion (RNE, ties to even) is
+    the same map; above 464 torch goes to NaN while the MX cast saturates
+    to +-448 (0x7E)."""
+    bits = finite_bf16_bits()
+    r = bf16_values(bits)
+    got = oracle_mod.cast_e4m3(r)
+    lib = torch.from_numpy(r.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    small = np.abs(r) <= 464
+    np.testing.assert_array_equal(got[small], lib[small])
+    big = ~small
+    np.testing.assert_array_equal(got[big], np.where(r[big] < 0, 0xFE, 0x7E))
+    # sign kept on zeros and on negatives that round to zero
+    assert oracle_mod.cast_e4m3([-0.0])[0] == 0x80
+    assert oracle_mod.cast_e4m3([-(2.0 ** -11)])[0] == 0x80
+
+
+def test_e4m3_cast_random_fp32_vs_torch(oracle_mod):
+    rng = np.random.default_rng(11)
+    r = (rng.standard_normal(200_000) * np.exp2(rng.integers(-14, 9, 200_000))).astype(np.float32)
+    r = r[np.abs(r) <= 464].astype(np.float64)
+    lib = torch.from_numpy(r.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle_mod.cast_e4m3(r), lib)
+
+
+def test_e4m3_cast_ties_by_hand(oracle_mod):
+    """Midpoints between neighbouring E4M3 values go to the even mantissa."""
+    cases = {
+        1.0625: 0x38,           # between 1.0 (M=0) and 1.125 (M=1) -> 1.0
+        1.1875: 0x3A,           # between 1.125 (M=1) and 1.25 (M=2) -> 1.25
+        2.0 ** -10: 0x00,       # half the smallest subnormal -> 0
+        3 * 2.0 ** -10: 0x02,   # between 1 and 2 subnormal steps -> 2
+        464.0: 0x7E,            # between 448 and 480 (not finite) -> 448
+        15 * 2.0 ** -10: 0x08,  # between 7/8*2^-6 (0x07) and 2^-6 (0x08) -> 0x08
+    }
+    got = oracle_mod.cast_e4m3(list(cases))
+    assert got.tolist() == list(cases.values())
+
+
+# ----------------------------------------------------------------- E2M1
+def test_e2m1_decode_table(oracle_mod):
+    assert [oracle_mod.decode_e2m1(c) for c in range(8)] == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    assert [oracle_mod.decode_e2m1(c) for c in range(8, 16)] == [-0.0, -0.5, -1, -1.5, -2, -3, -4, -6]
+
+
+def test_e2m1_cast_exhaustive_vs_ml_dtypes(oracle_mod):
+    """Every finite bf16 value and fp32 values one ulp around every tie point:
+    ml_dtypes' float4_e2m1fn conversion is a saturating RNE cast that keeps
+    the sign of zero, the same map."""
+    ml_dtypes = pytest.importorskip("ml_dtypes")
+    r = bf16_values(finite_bf16_bits())
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 7.0], np.float32)
+    near = np.concatenate([ties, np.nextafter(ties, np.float32(0)), np.nextafter(ties, np.float32(100))])
+    r = np.concatenate([r, near, -near]).astype(np.float32)
+    lib = r.astype(ml_dtypes.float4_e2m1fn).view(np.uint8) & 0xF
+    np.testing.assert_array_equal(oracle_mod.cast_e2m1(r.astype(np.float64)), lib)
+
+
+def test_e2m1_cast_by_hand(oracle_mod):
+    cases = {0.25: 0x0, 0.2500001: 0x1, 0.75: 0x2, 1.25: 0x2, 1.75: 0x4, 2.5: 0x4,
+             3.5: 0x6, 5.0: 0x6, 5.0001: 0x7, 100.0: 0x7, -0.1: 0x8, -6.5: 0xF}
+    assert oracle_mod.cast_e2m1(list(cases)).tolist() == list(cases.values())
+
+
+# ------------------------------------------------------------------ H16
+def test_h16_matches_sylvester_matrix_on_small_integers(oracle_mod):
+    """On small integers fp32 is exact, so the butterfly must equal the
+    explicit product (1/4) * H16 @ v with scipy's Sylvester Hadamard."""
+    from scipy.linalg import hadamard
+    Hm = hadamard(16).astype(np.float64)
+    rng = np.random.default_rng(3)
+    v = rng.integers(-1000, 1000, size=(64, 16)).astype(np.float32)
+    got = oracle_mod.h16(v).reshape(64, 16).astype(np.float64)
+    np.testing.assert_array_equal(got, (v.astype(np.float64) @ Hm.T) / 4.0)
+
+
+def test_h16_closed_forms(oracle_mod):
+    e0 = np.zeros(16, np.float32)
+    e0[0] = 1
+    np.testing.assert_array_equal(oracle_mod.h16(e0), np.full(16, 0.25, np.float32))
+    c = np.full(16, 3.0, np.float32)
+    want = np.zeros(16, np.float32)
+    want[0] = 12.0
+    np.testing.assert_array_equal(oracle_mod.h16(c), want)
+    # involution: ((1/4) H16)^2 = I, exact on small integers
+    v = np.arange(-8, 8, dtype=np.float32) * 4
+    np.testing.assert_array_equal(oracle_mod.h16(oracle_mod.h16(v)), v)
+
+
+def test_h16_preserves_norm(oracle_mod):
+    rng = np.random.default_rng(4)
+    v = rng.standard_normal((1000, 16)).astype(np.float32)
+    y = oracle_mod.h16(v).reshape(1000, 16)
+    np.testing.assert_allclose(np.linalg.norm(y.astype(np.float64), axis=1),
+                               np.linalg.norm(v.astype(np.float64), axis=1), rtol=1e-6)
+
+
+# --------------------------------------------------- estimator closed forms
+def const_row(value_bits, H):
+    return np.full((1, H), value_bits, np.uint16)
+
+
+@pytest.mark.parametrize("p", [1, 2])
+@pytest.mark.parametrize("bits", [0x3F80, 0x4040, 0xC2C8, 0x0001, 0x0080, 0x7F7F, 0x3C00])
+def test_constant_row_estimate_is_the_block_scale(oracle_mod, p, bits):
+    """A constant row has s_k = s for every block, so the power mean is s and
+    inv_rms = 1/s exactly for both p (the estimator formula with c = 1)."""
+    H = 256
+    codes, scales, inv = oracle_mod.mxnorm_quant(const_row(bits, H), p, "mxfp8")
+    amax = abs(float(synth.bf16_bits_to_f32(np.array([bits]))[0]))
+    e = max(-127, math.floor(math.log2(amax)) - 8)
+    assert (scales == e + 127).all()
+    assert inv[0] == np.float32(2.0 ** -e)
+
+
+@pytest.mark.parametrize("a,b", [(0, 0), (0, 3), (-5, 7), (-100, 90), (2, -60)])
+def test_two_level_row_closed_form(oracle_mod, a, b):
+    """Half the blocks with scale 2^a, half with 2^b:
+    M_1 = (2^a + 2^b)/2, M_2 = sqrt((4^a + 4^b)/2); inv_rms = RN_fp32(1/M_p)."""
+    H, K = 512, 16
+    x = np.zeros((1, H), np.float32)
+    x[0, : H // 2] = 2.0 ** (a + 8)     # amax 2^(a+8) -> e = a for E4M3
+    x[0, H // 2:] = 2.0 ** (b + 8)
+    xb = synth.f32_to_bf16_bits(x)
+    _, scales, inv1 = oracle_mod.mxnorm_quant(xb, 1, "mxfp8")
+    _, _, inv2 = oracle_mod.mxnorm_quant(xb, 2, "mxfp8")
+    assert scales[0, : K // 2].tolist() == [a + 127] * (K // 2)
+    assert scales[0, K // 2:].tolist() == [b + 127] * (K // 2)
+    m1 = (Fraction(2) ** a + Fraction(2) ** b) / 2
+    m2sq = (Fraction(4) ** a + Fraction(4) ** b) / 2
+    assert inv1[0] == np.float32(float(1 / m1))
+    want2 = 1.0 / math.sqrt(float(m2sq))
+    assert abs(float(inv2[0]) - want2) <= 0.5 * float(np.spacing(np.float32(want2)))
+
+
+@pytest.mark.parametrize("p", [1, 2])
+def test_single_nonzero_block(oracle_mod, p):
+    """One block at scale s, K-1 zero blocks at 2^-127:
+    M_p = ((s^p + (K-1) 2^(-127p)) / K)^(1/p) ~= K^(-1/p) s."""
+    H, K = 1024, 32
+    x = np.zeros((1, H), np.float32)
+    x[0, 40:72] = 3.0     # block 1 (elements 32..63) partly, block 2 partly
+    x[0, 32:64] = 3.0     # block 1 fully: amax 3 -> e = 1 - 8 = -7
+    x[0, 64:72] = 0.0
+    xb = synth.f32_to_bf16_bits(x)
+    _, scales, inv = oracle_mod.mxnorm_quant(xb, p, "mxfp8")
+    assert scales[0, 1] == 120 and (np.delete(scales[0], 1) == 0).all()
+    mp = ((Fraction(2) ** (-7 * p) + (K - 1) * Fraction(2) ** (-127 * p)) / K)
+    want = 1.0 / (float(mp) if p == 1 else math.sqrt(float(mp)))
+    assert abs(float(inv[0]) - want) <= 0.5 * float(np.spacing(np.float32(want)))
+    approx = K ** (1.0 / p) * 2.0 ** 7
+    assert abs(float(inv[0]) / approx - 1) < 1e-6
+
+
+def test_zero_row(oracle_mod):
+    x = np.zeros((2, 64), np.uint16)
+    x[1] = 0x8000  # -0
+    codes, scales, inv = oracle_mod.mxnorm_quant(x, 2, "mxfp8")
+    assert (scales == 0).all()
+    assert (codes[0] == 0).all() and (codes[1] == 0x80).all()
+    assert (inv == np.float32(2.0 ** 127)).all()
+
+
+def test_nonfinite_block_reading(oracle_mod):
+    x = synth.make_random_rows(2, 96, 1)
+    x[0, 40] = 0x7F80          # +Inf in block 1
+    x[1, 70] = 0x7FC0          # NaN in block 2
+    codes, scales, inv = oracle_mod.mxnorm_quant(x, 2, "mxfp8")
+    assert scales[0, 1] == 0xFF and (codes[0, 32:64] == 0x7F).all()
+    assert scales[1, 2] == 0xFF and (codes[1, 64:96] == 0x7F).all()
+    assert scales[0, 0] != 0xFF and scales[0, 2] != 0xFF
+    assert np.isnan(inv).all()
+    c4, s4, i4 = oracle_mod.mxnorm_quant(x, 2, "mxfp4")
+    assert s4[0, 1] == 0xFF and (c4[0, 16:32] == 0).all() and np.isnan(i4).all()
+
+
+# ----------------------------------------------------------- invariants
+@pytest.mark.parametrize("fmt,emax,qmax", [("mxfp8", 8, 448.0), ("mxfp4", 2, 6.0), ("mxfp4_h16", 2, 6.0)])
+@pytest.mark.parametrize("p", [1, 2])
+def test_cast_and_growth_invariants(oracle_mod, fmt, emax, qmax, p):
+    """|dec(q)| <= qmax; |dec(q) - x/s| <= half a grid step unless saturated;
+    saturation only when |x|/s > qmax; and the growth bound of the estimator,
+    |v_j| * inv_rms < K^(1/p) * 2^(emax+1) (section 4, Analisis de Picos:
+    O(K) growth for p = 1, tighter for p = 2)."""
+    w = synth.WORKLOADS["llama3_8b_65536x4096"]
+    x = synth.make_activations(w, rows=8)
+    codes, scales, inv = oracle_mod.mxnorm_quant(x, p, fmt)
+    K = w.K
+    v = synth.bf16_bits_to_f32(x).astype(np.float64)
+    if fmt == "mxfp4_h16":
+        v = oracle_mod.h16(v.astype(np.float32)).reshape(v.shape).astype(np.float64)
+    s = np.exp2(scales.astype(np.float64) - 127)
+    r = v / np.repeat(s, 32, axis=1)
+    if fmt == "mxfp8":
+        dec = np.vectorize(oracle_mod.decode_e4m3)(codes)
+        grid = np.array([oracle_mod.decode_e4m3(c) for c in range(127)])
+    else:
+        nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(codes.shape[0], -1)
+        dec = np.vectorize(oracle_mod.decode_e2m1)(nib)
+        grid = np.array([oracle_mod.decode_e2m1(c) for c in range(8)])
+    assert (np.abs(dec) <= qmax).all()
+    sat = np.abs(r) > qmax
+    assert (np.abs(dec[sat]) == qmax).all()
+    step = np.diff(grid)
+    idx = np.clip(np.searchsorted(grid, np.abs(r[~sat]), side="right") - 1, 0, len(step) - 1)
+    assert (np.abs(np.abs(dec[~sat]) - np.abs(r[~sat])) <= step[idx] / 2).all()
+    # amax/s lies in [2^emax, 2^(emax+1)) for non-zero blocks
+    amax = np.abs(v).reshape(v.shape[0], K, 32).max(-1)
+    assert ((amax / s >= 2.0 ** emax) & (amax / s < 2.0 ** (emax + 1))).all()
+    bound = K ** (1.0 / p) * 2.0 ** (emax + 1)
+    assert (np.abs(v) * inv[:, None].astype(np.float64) < bound).all()
+
+
+def test_growth_bound_is_tight_for_p1_with_one_outlier(oracle_mod):
+    """One huge element against tiny blocks: p = 1 lets |x| * inv approach
+    K * 2^(emax+1) while p = 2 stays below sqrt(K) * 2^(emax+1)."""
+    H, K = 4096, 128
+    x = np.full((1, H), 2.0 ** -100, np.float32)
+    x[0, 0] = 2.0 ** 20 * 1.99
+    xb = synth.f32_to_bf16_bits(x)
+    v = abs(float(synth.bf16_bits_to_f32(xb)[0, 0]))
+    _, _, inv1 = oracle_mod.mxnorm_quant(xb, 1, "mxfp8")
+    _, _, inv2 = oracle_mod.mxnorm_quant(xb, 2, "mxfp8")
+    assert v * float(inv1[0]) > 0.95 * K * 2.0 ** 9
+    assert v * float(inv2[0]) > 0.95 * math.sqrt(K) * 2.0 ** 9
+    assert v * float(inv2[0]) < math.sqrt(K) * 2.0 ** 9
+
+
+# ------------------------------------------------------ brute force rows
+def _check_rows_vs_bruteforce(oracle_mod, x, p, fmt):
+    from oracle import bruteforce as bf
+    codes, scales, inv = oracle_mod.mxnorm_quant(x, p, fmt)
+    for t in range(x.shape[0]):
+        bc, bs, bi = bf.mxnorm_row([int(b) for b in x[t]], p, fmt)
+        assert codes[t].tolist() == bc, (t, fmt, p)
+        assert scales[t].tolist() == bs, (t, fmt, p)
+        assert Fraction(float(inv[t])) == bi, (t, fmt, p, float(inv[t]), float(bi))
+
+
+def test_tiny_workload_vs_bruteforce(oracle_mod):
+    """The tiny oracle case (64 x 256, seed 0, N(0,1), channels 17 and 200
+    x50, MXFP8, p = 2) row by row against the exact-rational brute force."""
+    w = synth.WORKLOADS["tiny_64x256"]
+    _check_rows_vs_bruteforce(oracle_mod, synth.make_activations(w), 2, "mxfp8")
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "mxfp4_h16"])
+@pytest.mark.parametrize("p", [1, 2])
+@pytest.mark.parametrize("H", [32, 64, 96, 256])
+def test_random_tiny_rows_vs_bruteforce(oracle_mod, fmt, p, H):
+    rng = np.random.default_rng(H * 10 + p)
+    x = rng.standard_normal((3, H)).astype(np.float32) * np.exp2(rng.integers(-20, 20, (3, 1))).astype(np.float32)
+    x[:, rng.integers(0, H)] *= 40
+    _check_rows_vs_bruteforce(oracle_mod, synth.f32_to_bf16_bits(x), p, fmt)
+
+
+def test_subnormal_and_extreme_rows_vs_bruteforce(oracle_mod):
+    x = np.zeros((3, 64), np.uint16)
+    x[0] = np.arange(1, 65, dtype=np.uint16)            # bf16 subnormals
+    x[1] = 0x7F7F - np.arange(64, dtype=np.uint16)      # near the bf16 maximum
+    x[2, ::2] = 0x0001
+    x[2, 1::2] = 0x8003                                 # mixed-sign subnormals
+    for p in (1, 2):
+        _check_rows_vs_bruteforce(oracle_mod, x, p, "mxfp8")
+        _check_rows_vs_bruteforce(oracle_mod, x, p, "mxfp4")
+
+
+# --------------------------------------------------- RMSNorm baseline
+def test_rmsnorm_baseline_constant_rows(oracle_mod):
+    """Constant row c: RMS = |c|, inv = RN_fp32(1/sqrt(c^2 + eps))."""
+    for c in [1.0, -3.0, 0.5, 100.0]:
+        x = synth.f32_to_bf16_bits(np.full((1, 128), c, np.float32))
+        y, codes, scales, inv = oracle_mod.rmsnorm_mxfp8(x, 1e-5)
+        want = np.float32(1.0 / math.sqrt(c * c + 1e-5))
+        assert inv[0] == want
+        ref, _ = oracle_mod.mx_cast(y, "mxfp8")
+        assert (codes == ref).all()
+
+
+def test_rmsnorm_baseline_vs_torch_rms_norm(oracle_mod):
+    """y against torch.nn.functional.rms_norm in fp64 (library routine):
+    within one bf16 ulp (the oracle rounds x*inv to fp32 then to bf16)."""
+    x = synth.make_activations(synth.WORKLOADS["llama3_1b_32768x2048"], rows=4)
+    y, codes, scales, inv = oracle_mod.rmsnorm_mxfp8(x, 1e-5)
+    xt = torch.from_numpy(synth.bf16_bits_to_f32(x).astype(np.float64))
+    ref = torch.nn.functional.rms_norm(xt, (x.shape[1],), eps=1e-5).numpy()
+    yv = synth.bf16_bits_to_f32(y).astype(np.float64)
+    assert (np.abs(yv - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30).all()
+    rms = np.sqrt((synth.bf16_bits_to_f32(x).astype(np.float64) ** 2).mean(1) + 1e-5)
+    np.testing.assert_allclose(inv.astype(np.float64), 1 / rms, rtol=2 ** -24)
+    c2, s2 = oracle_mod.mx_cast(y, "mxfp8")
+    assert (c2 == codes).all() and (s2 == scales).all()
+
+
+def test_h16_rotation_preserves_row_rms(oracle_mod):
+    """H16/4 is orthonormal, so rotating a row keeps its RMS (the reason the
+    rotated path may feed the same estimator)."""
+    x = synth.make_activations(synth.WORKLOADS["llama3_8b_mxfp4_h16_65536x4096"], rows=4)
+    v = synth.bf16_bits_to_f32(x).astype(np.float32)
+    y = oracle_mod.h16(v).reshape(v.shape).astype(np.float64)
+    np.testing.assert_allclose(np.sqrt((y ** 2).mean(1)), np.sqrt((v.astype(np.float64) ** 2).mean(1)), rtol=1e-6)
