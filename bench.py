@@ -1,0 +1,447 @@
+#!/usr/bin/env python3
+"""Benchmark of libmxnorm's fused MXNorm pass on GB300.
+
+Headline: mxnorm_quant_fwd on the Llama-3-8B-shaped workload (x bf16
+[65536 x 4096], Student-t(4) x lognormal channel gain, 0.1% channels x100,
+MXFP8 E4M3, p = 2).  One step = one pass of the hot path over the batch:
+bf16 load, block absmax, E8M0 scale, E4M3 cast, power mean of the block
+scales, fp32 inverse-RMS estimate.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+value      tokens/s over all ranks, inputs resident in HBM, CUDA events on the
+           launching stream around every step; inputs (2 x 512 MiB, rotated)
+           exceed the 129 MB L2, so no flush is needed between steps.
+e2e        the same metric through the public API from pinned host buffers:
+           host->device copy of x, the C-ABI call, device->host copy of codes,
+           scales and inv_rms, every step inside the timed region.
+roofline   HBM-bound: algorithmic bytes per launch (2H + H + H/32 + 4 per row)
+           / mean per-launch time, against the measured HBM copy bandwidth.
+--impl reference   the CPU oracle (oracle/, test infrastructure) timed on a
+           bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "MXNorm+MXFP8 quantise tokens/s and HBM GB/s (% of GB300 peak), H=4096"
+WORKLOAD = "llama3_8b_65536x4096"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "mxnorm_warp_row_llama3_8b_65536x4096.md")
+
+
+def algorithmic_bytes(T: int, H: int, fmt: str) -> int:
+    code = H if fmt == "mxfp8" else H // 2
+    return T * (2 * H + code + H // 32 + 4)
+
+
+def baseline_bytes(T: int, H: int) -> int:
+    # kernel 1: read x, write y, write inv; kernel 2: read y, write codes + scales
+    return T * (2 * H + 2 * H + 4) + T * (2 * H + H + H // 32)
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mx_scale_reusing_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram read+write bytes per launch from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    try:
+        txt = open(PROFILE_TRAFFIC).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in txt.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_digest") != kernel_source_digest():
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {}, "fallback"
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (ctypes on the
+    driver's libnvidia-ml) every ~2 ms while running; read-only."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, index: int):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self._stop = threading.Event()
+        self._thr = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            self.handle = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.handle)) != 0:
+                raise OSError("no NVML handle")
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+        except OSError:
+            self.nvml = None
+
+    def _run(self):
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.handle, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.nvml is not None:
+            self._thr = threading.Thread(target=self._run, daemon=True)
+            self._thr.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._thr:
+            self._thr.join()
+
+    def summary(self):
+        if self.nvml is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml_unavailable"], "samples": 0}
+        names = [n for b, n in self.REASONS.items() if self.reasons & b]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------- GPU timing
+def time_launches(torch, stream, fn, steps: int, warmup: int, nbuf: int):
+    """fn(i) launches one step on `stream` using buffer set i % nbuf; returns
+    (per-launch ms list, region ms)."""
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            fn(i % nbuf)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            ev[i][0].record(stream)
+            fn(i % nbuf)
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in ev]
+    region = ev[0][0].elapsed_time(ev[-1][1])
+    return per, region
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import mx_scale_reusing_gb300 as mx
+    from mx_scale_reusing_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    mx.lib()
+
+    w = synth.WORKLOADS[WORKLOAD]
+    T, H, p = w.T, w.H, 2
+    xb = synth.make_activations(w)
+    x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16)
+    nbuf = 2
+    xs = [x_host.to(dev) for _ in range(nbuf)]
+    outs = [(torch.empty((T, H), dtype=torch.uint8, device=dev),
+             torch.empty((T, H // 32), dtype=torch.uint8, device=dev),
+             torch.empty((T,), dtype=torch.float32, device=dev)) for _ in range(nbuf)]
+    stream = torch.cuda.Stream(device=dev)
+    sptr = stream.cuda_stream
+
+    def step(i, p=p, variant=0):
+        c, s, v = outs[i]
+        mx.mxnorm_quant_fwd(xs[i].data_ptr(), T, H, p, 0, c.data_ptr(), s.data_ptr(), v.data_ptr(), sptr, variant)
+
+    # ---- headline: device-resident inputs, timed region bracketed by barrier + sync
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    with sampler:
+        per, region = time_launches(torch, stream, step, args.steps, args.warmup, nbuf)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_step = region / args.steps
+    mean_launch = statistics.fmean(per)
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    tokens_per_s = world * T / (ms_step * 1e-3)
+
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    abytes = algorithmic_bytes(T, H, "mxfp8")
+    achieved = abytes / (mean_launch * 1e-3) / 1e9
+
+    # ---- secondary measurements (same stream, fewer steps)
+    sec_steps = max(20, min(args.steps, 300))
+    extra = {}
+
+    def gbs(nbytes, ms):
+        return round(nbytes / (ms * 1e-3) / 1e9, 1)
+
+    per1, _ = time_launches(torch, stream, lambda i: step(i, p=1), sec_steps, 5, nbuf)
+    m = statistics.fmean(per1)
+    extra["mxnorm_mxfp8_p1_warp_row"] = {"ms": round(m, 5), "GB/s": gbs(abytes, m), "frac": round(gbs(abytes, m) / hbm_peak, 4)}
+    pert, _ = time_launches(torch, stream, lambda i: step(i, variant=2), sec_steps, 5, nbuf)
+    m = statistics.fmean(pert)
+    extra["mxnorm_mxfp8_p2_tiled_tma"] = {"ms": round(m, 5), "GB/s": gbs(abytes, m), "frac": round(gbs(abytes, m) / hbm_peak, 4)}
+    perw, _ = time_launches(torch, stream, lambda i: step(i, variant=1), sec_steps, 5, nbuf)
+    m = statistics.fmean(perw)
+    extra["mxnorm_mxfp8_p2_warp_row"] = {"ms": round(m, 5), "GB/s": gbs(abytes, m), "frac": round(gbs(abytes, m) / hbm_peak, 4)}
+
+    y_ws = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+
+    def base_step(i):
+        c, s, v = outs[i]
+        st = mx.lib().rmsnorm_mxfp8_ref_fwd(xs[i].data_ptr(), T, H, ctypes.c_float(1e-5), y_ws.data_ptr(),
+                                            c.data_ptr(), s.data_ptr(), v.data_ptr(), ctypes.c_void_p(sptr))
+        if st:
+            raise RuntimeError(mx.lib().mxnorm_last_error().decode())
+
+    perb, _ = time_launches(torch, stream, base_step, sec_steps, 5, nbuf)
+    mb = statistics.fmean(perb)
+    extra["two_pass_rmsnorm_mxfp8_baseline"] = {
+        "ms": round(mb, 5), "GB/s": gbs(baseline_bytes(T, H), mb),
+        "speedup_of_mxnorm_p2": round(mb / mean_launch, 3)}
+    del y_ws
+
+    if not args.skip_fp4:
+        w4 = synth.WORKLOADS["llama3_8b_mxfp4_h16_65536x4096"]
+        x4 = torch.from_numpy(synth.make_activations(w4).view(np.int16)).view(torch.bfloat16).to(dev)
+        c4 = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
+
+        def fp4_step(i):
+            c, s, v = outs[i]
+            mx.mxnorm_quant_fwd(x4.data_ptr(), T, H, 2, 2, c4.data_ptr(), s.data_ptr(), v.data_ptr(), sptr, 0)
+
+        per4, _ = time_launches(torch, stream, fp4_step, sec_steps, 5, nbuf)
+        m = statistics.fmean(per4)
+        b4 = algorithmic_bytes(T, H, "mxfp4")
+        extra["mxnorm_mxfp4_h16_p2"] = {"workload": "llama3_8b_mxfp4_h16_65536x4096", "ms": round(m, 5),
+                                        "GB/s": gbs(b4, m), "frac": round(gbs(b4, m) / hbm_peak, 4)}
+        del x4, c4
+
+    # ---- e2e through the public API from pinned host buffers
+    e2e = run_e2e(torch, mx, x_host, T, H, dev, args.e2e_steps)
+    if world > 1:
+        t = torch.tensor([e2e["ms_per_step"]], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["ms_per_step"] = float(t.item())
+    e2e_val = world * T / (e2e["ms_per_step"] * 1e-3)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(tokens_per_s, 1),
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 6),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic (seeded Student-t(4) x lognormal channel gain, 0.1% channels x100, bf16)",
+            "config": {"workload": WORKLOAD, "T": T, "H": H, "p": p, "fmt": "mxfp8_e4m3", "block": 32,
+                       "variant": "auto (warp_row)", "global_batch_tokens": world * T,
+                       "parallelism": f"replicas x{world} (rows shard, no collective)",
+                       "l2": "inputs larger than L2 (2 x 512 MiB rotated), no flush"},
+            "hbm_GBps": round(achieved, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(achieved / hbm_peak, 4), "traffic": profiled_traffic(),
+                         "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": abytes,
+                         "mean_launch_ms": round(mean_launch, 6)},
+            "clocks": sampler.summary(),
+            "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                    "ms_per_step": round(e2e["ms_per_step"], 4), "steps": e2e["steps"],
+                    "path": "mx.quant_fwd_host (pinned host -> HBM, C-ABI mxnorm_quant_fwd, HBM -> pinned host)"},
+            "gpu_launches": args.steps,
+            "secondary": extra,
+        }
+        if not args.skip_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(xb, p, args.cpu_rows)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(torch, mx, x_host, T, H, dev, steps):
+    x_pin = x_host.pin_memory()
+    c_pin = torch.empty((T, H), dtype=torch.uint8).pin_memory()
+    s_pin = torch.empty((T, H // 32), dtype=torch.uint8).pin_memory()
+    i_pin = torch.empty((T,), dtype=torch.float32).pin_memory()
+    out = (c_pin, s_pin, i_pin)
+    for _ in range(2):
+        mx.quant_fwd_host(x_pin, p=2, fmt="mxfp8", out=out, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        mx.quant_fwd_host(x_pin, p=2, fmt="mxfp8", out=out, device=dev)
+    torch.cuda.synchronize()
+    ms = (time.perf_counter() - t0) * 1e3 / steps
+    h2d = x_pin.numel() * 2
+    d2h = c_pin.numel() + s_pin.numel() + i_pin.numel() * 4
+    return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h, "steps": steps}
+
+
+def cpu_baseline(xb, p, rows):
+    """The oracle as it stands, single-threaded, on the first `rows` rows."""
+    import oracle
+    oracle.build()
+    sample = np.ascontiguousarray(xb[:rows])
+    t0 = time.perf_counter()
+    oracle.mxnorm_quant(sample, p, "mxfp8")
+    dt = time.perf_counter() - t0
+    return {"value": round(rows / dt, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} rows of {WORKLOAD} (H=4096, MXFP8, p={p}), {dt:.1f} s single-threaded"}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle on the machine's host cores, each step a
+    bounded sample of the workload; rank 0 only."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    from mx_scale_reusing_gb300 import synth
+    oracle.build()
+    w = synth.WORKLOADS[WORKLOAD]
+    total_rows_budget = 180_000          # ~100 s of single-core oracle work at H = 4096
+    rows = int(max(1, min(4096, total_rows_budget // max(1, args.steps + args.warmup))))
+    xb = synth.make_activations(w, rows=rows)
+    for _ in range(args.warmup):
+        oracle.mxnorm_quant(xb, 2, "mxfp8")
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.mxnorm_quant(xb, 2, "mxfp8")
+    dt = time.perf_counter() - t0
+    ms = dt * 1e3 / args.steps
+    val = rows / (ms * 1e-3)
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (same generator and seed as the GPU arm)",
+            "config": {"workload": WORKLOAD, "T": w.T, "H": w.H, "p": 2, "fmt": "mxfp8_e4m3",
+                       "rows_per_step": rows},
+            "cpu_baseline": {"value": round(val, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"first {rows} rows of {WORKLOAD} per step"},
+            "e2e": {"value": round(val, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_profile_case(args):
+    """A small case for ncu: the first N rows of the headline workload (or
+    of the MXFP4+H16 workload), one kernel, few launches."""
+    import torch
+
+    import mx_scale_reusing_gb300 as mx
+    from mx_scale_reusing_gb300 import synth
+    name = WORKLOAD if args.profile_fmt == "mxfp8" else "llama3_8b_mxfp4_h16_65536x4096"
+    w = synth.WORKLOADS[name]
+    T, H = args.profile_rows, w.H
+    x = torch.from_numpy(synth.make_activations(w, rows=T).view(np.int16)).view(torch.bfloat16).cuda()
+    stream = torch.cuda.Stream()
+    if args.profile_baseline:
+        y = torch.empty_like(x)
+
+        def fn(i):
+            mx.rmsnorm_mxfp8_ref_fwd(x, 1e-5, stream=stream, out=(y, codes, scales, inv))
+        codes = torch.empty((T, H), dtype=torch.uint8, device="cuda")
+    else:
+        codes = torch.empty((T, mx.code_bytes(H, args.profile_fmt)), dtype=torch.uint8, device="cuda")
+
+        def fn(i):
+            mx.quant_fwd(x, 2, args.profile_fmt, args.profile_variant, out=(codes, scales, inv), stream=stream)
+    scales = torch.empty((T, H // 32), dtype=torch.uint8, device="cuda")
+    inv = torch.empty((T,), dtype=torch.float32, device="cuda")
+    per, region = time_launches(torch, stream, fn, args.steps, args.warmup, 1)
+    nbytes = baseline_bytes(T, H) if args.profile_baseline else algorithmic_bytes(T, H, args.profile_fmt)
+    m = statistics.fmean(per)
+    print(json.dumps({"profile_only": True, "workload": name, "rows": T, "variant": args.profile_variant,
+                      "baseline": args.profile_baseline, "mean_launch_ms": round(m, 6),
+                      "GB/s": round(nbytes / (m * 1e-3) / 1e9, 1)}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="own", choices=["own", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-rows", type=int, default=12288)
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-fp4", action="store_true")
+    ap.add_argument("--profile-rows", type=int, default=0,
+                    help="profiling case: time only the headline kernel on the first N rows "
+                         "(its line carries profile_only; not a benchmark result)")
+    ap.add_argument("--profile-variant", default="auto", choices=["auto", "warp_row", "tiled_tma"])
+    ap.add_argument("--profile-fmt", default="mxfp8", choices=["mxfp8", "mxfp4_h16"])
+    ap.add_argument("--profile-baseline", action="store_true",
+                    help="profiling case: the two-pass baseline instead of MXNorm")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.profile_rows:
+        run_profile_case(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

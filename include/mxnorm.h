@@ -1,0 +1,138 @@
+/*
+ * mxnorm.h -- C ABI of libmxnorm: MXNorm's fused MX-quantise + scale-reuse
+ * inverse-RMS pass, and the two-pass RMSNorm-then-MXFP8 baseline, for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Method.  "MXNorm: Reusing MXFP block scales for efficient tensor
+ * normalisation" (gist.science summary), Resumen tecnico:
+ *   - 2. Metodologia, "Fundamentos Teoricos": the inverse RMS is estimated
+ *     as rho~ = c(p,B) * ((1/K) sum_{k=1..K} m~_k^p)^(-1/p) over the K = H/B
+ *     blocks of a row, p = 1 (arithmetic) or 2 (quadratic power mean);
+ *   - 2. Metodologia, "Implementacion": one fused pass computes the block
+ *     maxima, the estimate and the MX codes; the gain gamma is folded into
+ *     the next linear layer's weight (MXNormLinear), so no gamma here;
+ *   - the paper's English abstract: the RMS comes from the block scales of
+ *     the MXFP8 cast, a reduction 32x smaller than RMSNorm's.
+ * Encodings and the shared-exponent rule: OCP Microscaling Formats (MX)
+ * v1.0, sections 5 and 6.3.  MXFP4 with a deterministic 16x16 Hadamard
+ * rotation: "Entrenamiento Previo de Modelos de Lenguaje Grandes con MXFP4"
+ * (gist.science summary), Metodologia, item 3.
+ *
+ * What one call computes, per row of x (bf16, H elements, H % 32 == 0):
+ *   v      = x, or for MXFP4_E2M1_H16 the rotation (1/4) H16 applied to each
+ *            aligned group of 16 elements in fp32 (Sylvester order, butterfly
+ *            stages 1, 2, 4, 8, each add rounded to fp32, then * 1/4);
+ *   a_k    = max |v_j| over block k (32 elements), k = 0..K-1;
+ *   e_k    = max(floor(log2 a_k) - emax, -127), emax = 8 (E4M3) or 2 (E2M1),
+ *            e_k = -127 when a_k = 0;  scales[k] = e_k + 127 (E8M0);
+ *   codes  = saturating round-to-nearest-even of v_j * 2^-e_k in FP8 E4M3
+ *            (one byte per element) or FP4 E2M1 (two elements per byte,
+ *            element 2i in the LOW nibble); the sign of v_j is kept, so -0
+ *            and negatives that round to zero encode as 0x80 (E4M3) / 0x8;
+ *   inv_rms = ((1/K) sum_k 2^(p e_k))^(-1/p), fp32 (c(p,B) = 1: a caller
+ *            that wants the corrected estimate multiplies by c, e.g. folded
+ *            with gamma into the consumer weight).
+ * A block holding Inf or NaN gets scale 0xFF (E8M0 NaN), codes 0x7F (E4M3)
+ * or 0 (E2M1), and its row's inv_rms is NaN.
+ *
+ * Memory and ownership.  Every pointer is a DEVICE pointer owned by the
+ * caller; row-major, densely packed (row stride = row length):
+ *   x        bf16   [T, H]          16-byte aligned
+ *   codes    uint8  [T, H]  (E4M3)  16-byte aligned
+ *            uint8  [T, H/2] (E2M1, E2M1_H16)
+ *   scales   uint8  [T, H/32]       any alignment
+ *   inv_rms  float  [T]             4-byte aligned
+ * The library allocates no device memory, keeps no state between calls
+ * except a per-thread error string and a per-device launch-shape cache, and
+ * never synchronises: work is queued on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and the call returns.  Outputs are fully
+ * written when the stream reaches the kernel's end; after an error return
+ * they are unspecified.  Inputs and outputs must not overlap.
+ *
+ * Errors.  Arguments are checked on the host before any launch:
+ *   T < 0, H <= 0, H % 32 != 0, p not in {1, 2}, unknown fmt or variant,
+ *   a NULL pointer                              -> MXNORM_ERR_INVALID_ARG
+ *   H > MXNORM_MAX_H, or a variant that does not
+ *   support the shape                           -> MXNORM_ERR_UNSUPPORTED
+ *   a pointer below its alignment               -> MXNORM_ERR_MISALIGNED
+ *   a CUDA launch error                         -> MXNORM_ERR_CUDA
+ * T == 0 returns MXNORM_OK and launches nothing.  mxnorm_last_error() gives
+ * the calling thread's last message.  There is no CPU fallback.
+ */
+#ifndef MXNORM_H_
+#define MXNORM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MXNORM_BLOCK 32
+#define MXNORM_MAX_H (1 << 20)
+#define MXNORM_ABI_VERSION 1
+
+typedef enum {
+  MXNORM_FMT_MXFP8_E4M3 = 0,     /* FP8 E4M3 codes, one byte per element     */
+  MXNORM_FMT_MXFP4_E2M1 = 1,     /* FP4 E2M1 codes, two per byte             */
+  MXNORM_FMT_MXFP4_E2M1_H16 = 2  /* (1/4) H16 rotation, then FP4 E2M1 codes  */
+} mxnorm_fmt;
+
+typedef enum {
+  MXNORM_OK = 0,
+  MXNORM_ERR_INVALID_ARG = 1,
+  MXNORM_ERR_UNSUPPORTED = 2,
+  MXNORM_ERR_MISALIGNED = 3,
+  MXNORM_ERR_CUDA = 4
+} mxnorm_status;
+
+typedef enum {
+  MXNORM_VARIANT_AUTO = 0,       /* the library picks                        */
+  MXNORM_VARIANT_WARP_ROW = 1,   /* one warp per row, vector loads            */
+  MXNORM_VARIANT_TILED_TMA = 2   /* row tiles staged in shared memory by bulk
+                                    async copies (TMA engine), persistent CTAs */
+} mxnorm_variant;
+
+/* MXNorm forward: MX codes + E8M0 scales + fp32 inverse-RMS estimate of
+ * every row of x, in one pass over x (the estimator of "Fundamentos
+ * Teoricos" evaluated on the scales of the cast, see above).
+ * p: 1 or 2.  fmt: an mxnorm_fmt.  stream: cudaStream_t or NULL. */
+int mxnorm_quant_fwd(const void* x, int64_t T, int64_t H, int p, int fmt, void* codes,
+                     uint8_t* scales, float* inv_rms, void* stream);
+
+/* As mxnorm_quant_fwd, with an explicit kernel variant (mxnorm_variant).
+ * Every variant writes bit-identical outputs. */
+int mxnorm_quant_fwd_ex(const void* x, int64_t T, int64_t H, int p, int fmt, void* codes,
+                        uint8_t* scales, float* inv_rms, int variant, void* stream);
+
+/* Two-pass baseline: the unfused pipeline MXNorm replaces ("MXNorm ...",
+ * Resumen tecnico, section 1: RMSNorm and the MXFP8 cast as separate
+ * operations).  Kernel 1: inv = 1/sqrt(mean(x^2) + eps) (fp32 sum, fp64
+ * root), y = bf16(fp32(x * inv)) written to y_workspace, inv to inv_rms.
+ * Kernel 2: MXFP8 E4M3 cast of y (same rules as above) into codes/scales.
+ * y_workspace: bf16 [T, H], 16-byte aligned, caller-owned; it holds y on
+ * return.  No gain (gamma = 1). */
+int rmsnorm_mxfp8_ref_fwd(const void* x, int64_t T, int64_t H, float eps, void* y_workspace,
+                          uint8_t* codes, uint8_t* scales, float* inv_rms, void* stream);
+
+/* Static text for a status code. */
+const char* mxnorm_status_string(int status);
+
+/* The calling thread's last error message ("" if none). */
+const char* mxnorm_last_error(void);
+
+/* MXNORM_ABI_VERSION of the loaded library. */
+int mxnorm_abi_version(void);
+
+/* Device-side error word of the current device, or'ed by kernels whose
+ * bounded waits gave up (bit 0: a shared-memory pipeline wait of the tiled
+ * variant timed out; its outputs for the affected rows are then invalid).
+ * Synchronous: copies the word to *flags (and zeroes it when clear != 0).
+ * Call after the work in question has completed. */
+int mxnorm_device_errors(uint32_t* flags, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXNORM_H_ */

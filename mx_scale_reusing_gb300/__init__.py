@@ -1,0 +1,206 @@
+"""libmxnorm Python binding: argument marshalling over the C ABI.
+
+Every step of the computation runs in the CUDA library (libmxnorm.so, built
+in-tree by ``mx_scale_reusing_gb300._build``); this module only checks
+tensors, allocates outputs with torch and passes raw device pointers plus the
+current CUDA stream.  There is no CPU fallback: without the built library
+every call raises ``MXNormLibraryMissing``.
+
+Method: "MXNorm: Reusing MXFP block scales for efficient tensor
+normalisation", Resumen tecnico, 2. Metodologia ("Fundamentos Teoricos":
+inverse RMS from the power mean of the MX block scales; "Implementacion":
+one fused pass).  The function names follow the C ABI in include/mxnorm.h.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "FMT", "VARIANT", "MXNormError", "MXNormLibraryMissing", "lib", "library_path",
+    "mxnorm_quant_fwd", "quant_fwd", "quant_fwd_host", "rmsnorm_mxfp8_ref_fwd", "device_errors",
+    "code_bytes",
+]
+
+FMT = {"mxfp8": 0, "mxfp4": 1, "mxfp4_h16": 2}
+VARIANT = {"auto": 0, "warp_row": 1, "tiled_tma": 2}
+STATUS = {0: "MXNORM_OK", 1: "MXNORM_ERR_INVALID_ARG", 2: "MXNORM_ERR_UNSUPPORTED",
+          3: "MXNORM_ERR_MISALIGNED", 4: "MXNORM_ERR_CUDA"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libmxnorm.so")
+_lib = None
+
+
+class MXNormLibraryMissing(RuntimeError):
+    pass
+
+
+class MXNormError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises MXNormLibraryMissing if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(library_path):
+        raise MXNormLibraryMissing(
+            f"{library_path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(library_path)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.mxnorm_quant_fwd.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp, vp]
+    L.mxnorm_quant_fwd.restype = i32
+    L.mxnorm_quant_fwd_ex.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp, i32, vp]
+    L.mxnorm_quant_fwd_ex.restype = i32
+    L.rmsnorm_mxfp8_ref_fwd.argtypes = [vp, i64, i64, ctypes.c_float, vp, vp, vp, vp, vp]
+    L.rmsnorm_mxfp8_ref_fwd.restype = i32
+    L.mxnorm_status_string.argtypes = [i32]
+    L.mxnorm_status_string.restype = ctypes.c_char_p
+    L.mxnorm_last_error.argtypes = []
+    L.mxnorm_last_error.restype = ctypes.c_char_p
+    L.mxnorm_abi_version.restype = i32
+    L.mxnorm_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+    L.mxnorm_device_errors.restype = i32
+    _lib = L
+    return L
+
+
+def _check(status: int):
+    if status != 0:
+        raise MXNormError(status, lib().mxnorm_last_error().decode())
+
+
+def code_bytes(H: int, fmt: str) -> int:
+    return H if FMT[fmt] == 0 else H // 2
+
+
+def _stream_ptr(device, stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def mxnorm_quant_fwd(x_ptr: int, T: int, H: int, p: int, fmt: int, codes_ptr: int, scales_ptr: int,
+                     inv_rms_ptr: int, stream_ptr: int = 0, variant: int = 0) -> None:
+    """Raw C-ABI call on device pointers (ints); raises MXNormError."""
+    _check(lib().mxnorm_quant_fwd_ex(x_ptr, T, H, p, fmt, codes_ptr, scales_ptr, inv_rms_ptr,
+                                     variant, stream_ptr))
+
+
+def quant_fwd(x, p: int = 2, fmt: str = "mxfp8", variant: str = "auto", out=None, stream=None):
+    """MXNorm forward of a contiguous bf16 CUDA tensor x [..., H].
+
+    Returns (codes uint8 [..., H or H/2], scales uint8 [..., H/32],
+    inv_rms float32 [...]).  `out` may pass preallocated tensors in that
+    order.  Runs on `stream` (default: the current stream); asynchronous.
+    """
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous bfloat16 CUDA tensor")
+    H = x.shape[-1]
+    T = x.numel() // H if H else 0
+    lead = tuple(x.shape[:-1])
+    if out is None:
+        codes = torch.empty(lead + (code_bytes(H, fmt),), dtype=torch.uint8, device=x.device)
+        scales = torch.empty(lead + (H // 32,), dtype=torch.uint8, device=x.device)
+        inv = torch.empty(lead, dtype=torch.float32, device=x.device)
+    else:
+        codes, scales, inv = out
+    _check(lib().mxnorm_quant_fwd_ex(x.data_ptr(), T, H, int(p), FMT[fmt], codes.data_ptr(),
+                                     scales.data_ptr(), inv.data_ptr(), VARIANT[variant],
+                                     _stream_ptr(x.device, stream)))
+    return codes, scales, inv
+
+
+def rmsnorm_mxfp8_ref_fwd(x, eps: float = 1e-5, out=None, stream=None):
+    """Two-pass RMSNorm-then-MXFP8 baseline.  Returns (y bf16 workspace,
+    codes uint8, scales uint8, inv_rms float32)."""
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous bfloat16 CUDA tensor")
+    H = x.shape[-1]
+    T = x.numel() // H if H else 0
+    lead = tuple(x.shape[:-1])
+    if out is None:
+        y = torch.empty_like(x)
+        codes = torch.empty(lead + (H,), dtype=torch.uint8, device=x.device)
+        scales = torch.empty(lead + (H // 32,), dtype=torch.uint8, device=x.device)
+        inv = torch.empty(lead, dtype=torch.float32, device=x.device)
+    else:
+        y, codes, scales, inv = out
+    _check(lib().rmsnorm_mxfp8_ref_fwd(x.data_ptr(), T, H, float(eps), y.data_ptr(), codes.data_ptr(),
+                                       scales.data_ptr(), inv.data_ptr(), _stream_ptr(x.device, stream)))
+    return y, codes, scales, inv
+
+
+def device_errors(clear: bool = True) -> int:
+    """The device error word (bit 0: a bounded pipeline wait timed out)."""
+    v = ctypes.c_uint32(0)
+    _check(lib().mxnorm_device_errors(ctypes.byref(v), int(clear)))
+    return v.value
+
+
+_host_ws = {}
+
+
+def quant_fwd_host(x, p: int = 2, fmt: str = "mxfp8", out=None, device=None, chunks: int = 8,
+                   variant: str = "auto"):
+    """MXNorm forward of a bf16 CPU tensor (pinned for full copy speed).
+
+    The rows are split into `chunks` pieces over three CUDA streams: per
+    piece a host->device copy of x, the C-ABI call, and device->host copies
+    of codes, scales and inv_rms, so copies in both directions overlap with
+    each other and with the kernels.  Device staging buffers are cached per
+    (device, shape, fmt).  Returns (codes, scales, inv_rms) CPU tensors,
+    valid once the current stream of `device` has synchronised.
+    """
+    import torch
+    if x.is_cuda or x.dtype != torch.bfloat16 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bfloat16 CPU tensor")
+    device = torch.device(device if device is not None else "cuda")
+    if device.index is None:
+        device = torch.device("cuda", torch.cuda.current_device())
+    H = x.shape[-1]
+    T = x.numel() // H if H else 0
+    cb = code_bytes(H, fmt)
+    if out is None:
+        out = (torch.empty((T, cb), dtype=torch.uint8).pin_memory(),
+               torch.empty((T, H // 32), dtype=torch.uint8).pin_memory(),
+               torch.empty((T,), dtype=torch.float32).pin_memory())
+    oc, os_, oi = (t.view(-1) for t in out)
+    key = (device.index, T, H, fmt)
+    ws = _host_ws.get(key)
+    if ws is None:
+        ws = {"x": torch.empty((T, H), dtype=torch.bfloat16, device=device),
+              "c": torch.empty((T, cb), dtype=torch.uint8, device=device),
+              "s": torch.empty((T, H // 32), dtype=torch.uint8, device=device),
+              "i": torch.empty((T,), dtype=torch.float32, device=device),
+              "streams": [torch.cuda.Stream(device=device) for _ in range(3)]}
+        _host_ws[key] = ws
+    xv = x.view(T, H)
+    cur = torch.cuda.current_stream(device)
+    streams = ws["streams"]
+    for s in streams:
+        s.wait_stream(cur)
+    rc = max(1, -(-T // max(1, chunks)))
+    L = lib()
+    for j, r0 in enumerate(range(0, T, rc)):
+        r1 = min(T, r0 + rc)
+        s = streams[j % len(streams)]
+        with torch.cuda.stream(s):
+            xd = ws["x"][r0:r1]
+            xd.copy_(xv[r0:r1], non_blocking=True)
+            cd, sd, idd = ws["c"][r0:r1], ws["s"][r0:r1], ws["i"][r0:r1]
+            _check(L.mxnorm_quant_fwd_ex(xd.data_ptr(), r1 - r0, H, int(p), FMT[fmt], cd.data_ptr(),
+                                         sd.data_ptr(), idd.data_ptr(), VARIANT[variant],
+                                         ctypes.c_void_p(s.cuda_stream)))
+            oc[r0 * cb:r1 * cb].copy_(cd.reshape(-1), non_blocking=True)
+            os_[r0 * (H // 32):r1 * (H // 32)].copy_(sd.reshape(-1), non_blocking=True)
+            oi[r0:r1].copy_(idd, non_blocking=True)
+    for s in streams:
+        cur.wait_stream(s)
+    return out

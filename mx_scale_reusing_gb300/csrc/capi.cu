@@ -1,0 +1,150 @@
+// capi.cu -- the extern "C" boundary of libmxnorm: argument validation,
+// variant selection and launches.  Declarations and the full contract are
+// in include/mxnorm.h.
+#include <cstdarg>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "launch.h"
+#include "mx_device.cuh"
+#include "mxnorm.h"
+
+namespace mxnorm {
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return status;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+std::mutex g_grid_mu;
+std::map<std::tuple<int, const void*, int, size_t>, int> g_grid_cache;  // -> CTAs per device fill
+
+int cuda_fail(cudaError_t err, const char* what) {
+  return fail(MXNORM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+int check_common(const void* x, int64_t T, int64_t H, const void* codes, const void* scales,
+                 const void* inv_rms) {
+  if (T < 0) return fail(MXNORM_ERR_INVALID_ARG, "T = %lld < 0", (long long)T);
+  if (H <= 0 || H % kBlock != 0)
+    return fail(MXNORM_ERR_INVALID_ARG, "H = %lld is not a positive multiple of 32", (long long)H);
+  if (H > MXNORM_MAX_H)
+    return fail(MXNORM_ERR_UNSUPPORTED, "H = %lld exceeds MXNORM_MAX_H = %d", (long long)H, MXNORM_MAX_H);
+  if (T == 0) return MXNORM_OK;
+  if (!x || !codes || !scales || !inv_rms) return fail(MXNORM_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(x, 16)) return fail(MXNORM_ERR_MISALIGNED, "x is not 16-byte aligned");
+  if (!aligned(codes, 16)) return fail(MXNORM_ERR_MISALIGNED, "codes is not 16-byte aligned");
+  if (!aligned(inv_rms, 4)) return fail(MXNORM_ERR_MISALIGNED, "inv_rms is not 4-byte aligned");
+  return MXNORM_OK;
+}
+
+}  // namespace
+
+int persistent_grid(const void* kernel, int threads, int64_t work_ctas, size_t dyn_smem) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, kernel, threads, dyn_smem);
+  int fill = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_grid_mu);
+    auto it = g_grid_cache.find(key);
+    if (it != g_grid_cache.end()) fill = it->second;
+  }
+  if (fill == 0) {
+    int sms = 0, per_sm = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, dyn_smem);
+    fill = (sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+    std::lock_guard<std::mutex> lk(g_grid_mu);
+    g_grid_cache[key] = fill;
+  }
+  int64_t g = work_ctas < fill ? work_ctas : fill;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace mxnorm
+
+using namespace mxnorm;
+
+extern "C" {
+
+int mxnorm_quant_fwd_ex(const void* x, int64_t T, int64_t H, int p, int fmt, void* codes,
+                        uint8_t* scales, float* inv_rms, int variant, void* stream) {
+  g_last_error.clear();
+  if (p != 1 && p != 2) return fail(MXNORM_ERR_INVALID_ARG, "p = %d is not 1 or 2", p);
+  if (fmt != MXNORM_FMT_MXFP8_E4M3 && fmt != MXNORM_FMT_MXFP4_E2M1 && fmt != MXNORM_FMT_MXFP4_E2M1_H16)
+    return fail(MXNORM_ERR_INVALID_ARG, "unknown fmt %d", fmt);
+  if (variant < MXNORM_VARIANT_AUTO || variant > MXNORM_VARIANT_TILED_TMA)
+    return fail(MXNORM_ERR_INVALID_ARG, "unknown variant %d", variant);
+  int st = check_common(x, T, H, codes, scales, inv_rms);
+  if (st != MXNORM_OK || T == 0) return st;
+  if (variant == MXNORM_VARIANT_TILED_TMA && !tiled_supported(H, fmt))
+    return fail(MXNORM_ERR_UNSUPPORTED, "tiled variant does not support H = %lld", (long long)H);
+
+  WarpRowArgs a{x, T, H, p, fmt, codes, scales, inv_rms};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool use_tiled = variant == MXNORM_VARIANT_TILED_TMA;
+  cudaError_t err = use_tiled ? launch_mxnorm_tiled(TiledArgs{a, nullptr}, s)
+                              : launch_mxnorm_warp_row(a, s);
+  if (err != cudaSuccess) return cuda_fail(err, "mxnorm_quant_fwd launch");
+  return MXNORM_OK;
+}
+
+int mxnorm_quant_fwd(const void* x, int64_t T, int64_t H, int p, int fmt, void* codes,
+                     uint8_t* scales, float* inv_rms, void* stream) {
+  return mxnorm_quant_fwd_ex(x, T, H, p, fmt, codes, scales, inv_rms, MXNORM_VARIANT_AUTO, stream);
+}
+
+int rmsnorm_mxfp8_ref_fwd(const void* x, int64_t T, int64_t H, float eps, void* y_workspace,
+                          uint8_t* codes, uint8_t* scales, float* inv_rms, void* stream) {
+  g_last_error.clear();
+  if (!(eps >= 0.0f)) return fail(MXNORM_ERR_INVALID_ARG, "eps must be >= 0");
+  int st = check_common(x, T, H, codes, scales, inv_rms);
+  if (st != MXNORM_OK || T == 0) return st;
+  if (!y_workspace) return fail(MXNORM_ERR_INVALID_ARG, "NULL y_workspace");
+  if (!aligned(y_workspace, 16)) return fail(MXNORM_ERR_MISALIGNED, "y_workspace is not 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err = launch_rmsnorm_bf16(RmsNormArgs{x, T, H, eps, y_workspace, inv_rms}, s);
+  if (err != cudaSuccess) return cuda_fail(err, "rmsnorm kernel launch");
+  err = launch_mx_cast_warp_row(WarpRowArgs{y_workspace, T, H, 2, MXNORM_FMT_MXFP8_E4M3, codes, scales, nullptr}, s);
+  if (err != cudaSuccess) return cuda_fail(err, "mxfp8 cast kernel launch");
+  return MXNORM_OK;
+}
+
+const char* mxnorm_status_string(int status) {
+  switch (status) {
+    case MXNORM_OK: return "MXNORM_OK";
+    case MXNORM_ERR_INVALID_ARG: return "MXNORM_ERR_INVALID_ARG";
+    case MXNORM_ERR_UNSUPPORTED: return "MXNORM_ERR_UNSUPPORTED";
+    case MXNORM_ERR_MISALIGNED: return "MXNORM_ERR_MISALIGNED";
+    case MXNORM_ERR_CUDA: return "MXNORM_ERR_CUDA";
+    default: return "MXNORM_ERR_UNKNOWN";
+  }
+}
+
+const char* mxnorm_last_error(void) { return g_last_error.c_str(); }
+
+int mxnorm_abi_version(void) { return MXNORM_ABI_VERSION; }
+
+int mxnorm_device_errors(uint32_t* flags, int clear) {
+  if (!flags) return fail(MXNORM_ERR_INVALID_ARG, "NULL flags");
+  cudaError_t err = read_device_error_word(flags, clear != 0);
+  if (err != cudaSuccess) return cuda_fail(err, "reading the device error word");
+  return MXNORM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,49 @@
+// launch.h -- internal launcher interface between the C ABI (capi.cu) and
+// the kernel translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxnorm {
+
+struct WarpRowArgs {
+  const void* x;      // bf16 [T, H]
+  int64_t T;
+  int64_t H;
+  int p;              // 1 or 2 (ignored by the cast-only form)
+  int fmt;            // Fmt
+  void* codes;        // u8 [T, H] (E4M3) or [T, H/2] (E2M1)
+  uint8_t* scales;    // u8 [T, H/32]
+  float* inv_rms;     // f32 [T] (unused by the cast-only form)
+};
+
+struct RmsNormArgs {
+  const void* x;      // bf16 [T, H]
+  int64_t T;
+  int64_t H;
+  float eps;
+  void* y;            // bf16 [T, H]
+  float* inv_rms;     // f32 [T]
+};
+
+struct TiledArgs {
+  WarpRowArgs base;
+  unsigned int* error_flag;  // device word set when a bounded wait gives up
+};
+
+// Grid size for a grid-stride kernel: enough CTAs to fill every SM at the
+// kernel's occupancy, never more than `work_ctas`.  Cached per device.
+int persistent_grid(const void* kernel, int threads_per_cta, int64_t work_ctas,
+                    size_t dyn_smem = 0);
+
+cudaError_t launch_mxnorm_warp_row(const WarpRowArgs& a, cudaStream_t s);
+cudaError_t launch_mx_cast_warp_row(const WarpRowArgs& a, cudaStream_t s);
+cudaError_t launch_rmsnorm_bf16(const RmsNormArgs& a, cudaStream_t s);
+cudaError_t launch_mxnorm_tiled(const TiledArgs& a, cudaStream_t s);
+bool tiled_supported(int64_t H, int fmt);
+
+// Copy (and optionally zero) the device error word that bounded waits set.
+cudaError_t read_device_error_word(uint32_t* out, bool clear);
+
+}  // namespace mxnorm

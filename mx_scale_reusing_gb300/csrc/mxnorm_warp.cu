@@ -1,0 +1,106 @@
+// mxnorm_warp.cu -- one-row-per-warp MXNorm kernel (and the cast-only form
+// used by the two-pass baseline's second kernel).
+//
+// Work split: each warp owns whole rows (grid-stride over T).  A row is
+// walked in chunks of 32 * VEC elements; lane l of chunk c holds elements
+// [c*32*VEC + l*VEC, +VEC) -- one 16-byte (VEC = 8) or 32-byte (VEC = 16)
+// coalesced load, so a warp reads 512 B or 1 KiB contiguous per chunk.  An
+// MX block (32 elements) is 32/VEC lanes, its absmax a 1-2 step xor
+// shuffle.  With the chunk count known at compile time every load of a row
+// is issued before any arithmetic, which keeps up to 8 KiB per warp in
+// flight.  Per block the lead lane writes the E8M0 byte and feeds the
+// power-mean accumulator; the row's accumulators meet in a warp reduction
+// and lane 0 writes inv_rms.
+//
+// Method: "MXNorm: Reusing MXFP block scales for efficient tensor
+// normalisation", Resumen tecnico, 2. Metodologia: "Fundamentos Teoricos"
+// (rho~ = c(p,B) ((1/K) sum_k m~_k^p)^(-1/p), read with m~_k = s_k, c = 1)
+// and "Implementacion" (the block maxima of the cast feed the estimate in
+// one pass); OCP MX v1.0 6.3 for the cast.
+#include "launch.h"
+#include "mx_row.cuh"
+
+namespace mxnorm {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+
+template <int FMT, int VEC, int NCHUNK, bool LOAD32, bool ESTIMATE>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+    mx_warp_row_kernel(const uint16_t* __restrict__ x, int64_t T, int H,
+                       uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                       float* __restrict__ inv_rms, int p) {
+  using Tr = FmtTraits<FMT>;
+  const int K = H / kBlock;
+  const int64_t code_row = Tr::fp4 ? (int64_t)(H / 2) : (int64_t)H;
+  const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+  for (int64_t row = warp0; row < T; row += nwarps) {
+    const uint16_t* xr = x + row * (int64_t)H;
+    auto load = [xr](int e0, uint32_t (&w)[VEC / 2]) { load_lane<VEC, LOAD32>(xr + e0, w); };
+    mx_row<FMT, VEC, NCHUNK, ESTIMATE>(load, H, p, codes + row * code_row, scales + row * (int64_t)K,
+                                       inv_rms + row);
+  }
+}
+
+template <int FMT, int VEC, int NCHUNK, bool LOAD32, bool ESTIMATE>
+cudaError_t launch_one(const WarpRowArgs& a, cudaStream_t stream) {
+  auto kern = mx_warp_row_kernel<FMT, VEC, NCHUNK, LOAD32, ESTIMATE>;
+  const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kWarpsPerCta * 32,
+                                   (a.T + kWarpsPerCta - 1) / kWarpsPerCta);
+  kern<<<grid, kWarpsPerCta * 32, 0, stream>>>(static_cast<const uint16_t*>(a.x), a.T, (int)a.H,
+                                               static_cast<uint8_t*>(a.codes), a.scales,
+                                               a.inv_rms, a.p);
+  return cudaGetLastError();
+}
+
+template <int FMT, int VEC, bool LOAD32, bool ESTIMATE>
+cudaError_t launch_by_h(const WarpRowArgs& a, cudaStream_t s) {
+  const int64_t CE = 32 * VEC;
+  const int64_t n = (a.H + CE - 1) / CE;
+  switch (n) {
+    case 1: return launch_one<FMT, VEC, 1, LOAD32, ESTIMATE>(a, s);
+    case 2: return launch_one<FMT, VEC, 2, LOAD32, ESTIMATE>(a, s);
+    case 3: return launch_one<FMT, VEC, 3, LOAD32, ESTIMATE>(a, s);
+    case 4: return launch_one<FMT, VEC, 4, LOAD32, ESTIMATE>(a, s);
+    case 8: return launch_one<FMT, VEC, 8, LOAD32, ESTIMATE>(a, s);
+    case 16: return launch_one<FMT, VEC, 16, LOAD32, ESTIMATE>(a, s);
+    default: return launch_one<FMT, VEC, 0, LOAD32, ESTIMATE>(a, s);
+  }
+}
+
+template <int FMT, bool ESTIMATE>
+cudaError_t launch_fmt(const WarpRowArgs& a, cudaStream_t s) {
+  const bool x32 = (reinterpret_cast<uintptr_t>(a.x) & 31) == 0;
+  // 32-byte lanes when a chunk of 512 elements tiles the row (or when the
+  // H16 rotation needs a whole 16-group per lane), else 16-byte lanes.
+  const bool vec16 = FmtTraits<FMT>::h16 || (a.H % 512 == 0);
+  if (vec16) {
+    if (x32) return launch_by_h<FMT, 16, true, ESTIMATE>(a, s);
+    return launch_by_h<FMT, 16, false, ESTIMATE>(a, s);
+  }
+  if constexpr (!FmtTraits<FMT>::h16) return launch_by_h<FMT, 8, false, ESTIMATE>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_mxnorm_warp_row(const WarpRowArgs& a, cudaStream_t s) {
+  switch (a.fmt) {
+    case kFmtE4M3: return launch_fmt<kFmtE4M3, true>(a, s);
+    case kFmtE2M1: return launch_fmt<kFmtE2M1, true>(a, s);
+    case kFmtE2M1H16: return launch_fmt<kFmtE2M1H16, true>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_mx_cast_warp_row(const WarpRowArgs& a, cudaStream_t s) {
+  switch (a.fmt) {
+    case kFmtE4M3: return launch_fmt<kFmtE4M3, false>(a, s);
+    case kFmtE2M1: return launch_fmt<kFmtE2M1, false>(a, s);
+    case kFmtE2M1H16: return launch_fmt<kFmtE2M1H16, false>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mxnorm

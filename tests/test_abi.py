@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI: the library loads, exports every function
+include/mxnorm.h declares, and rejects bad arguments with the documented
+status before touching the GPU (these calls never reach a CUDA API)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mx_scale_reusing_gb300 as mx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mx_scale_reusing_gb300 import _build
+    _build.build()
+    return mx.lib()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert {"mxnorm_quant_fwd", "mxnorm_quant_fwd_ex", "rmsnorm_mxfp8_ref_fwd"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_abi_version_and_strings(L):
+    assert L.mxnorm_abi_version() == 1
+    assert L.mxnorm_status_string(0) == b"MXNORM_OK"
+    assert L.mxnorm_status_string(3) == b"MXNORM_ERR_MISALIGNED"
+    assert L.mxnorm_status_string(99) == b"MXNORM_ERR_UNKNOWN"
+
+
+FAKE = 1 << 40  # never dereferenced: validation fails or T == 0 first
+
+
+@pytest.mark.parametrize("T,H,p,fmt,variant,status", [
+    (0, 4096, 2, 0, 0, 0),            # empty input: no-op
+    (-1, 4096, 2, 0, 0, 1),
+    (8, 0, 2, 0, 0, 1),
+    (8, 33, 2, 0, 0, 1),
+    (8, 4096, 3, 0, 0, 1),
+    (8, 4096, 0, 0, 0, 1),
+    (8, 4096, 2, 7, 0, 1),
+    (8, 4096, 2, 0, 9, 1),
+    (8, (1 << 20) + 32, 2, 0, 0, 2),   # above MXNORM_MAX_H
+    (8, 8192, 2, 0, 2, 2),            # tiled variant does not take H = 8192
+])
+def test_quant_fwd_validation(L, T, H, p, fmt, variant, status):
+    rc = L.mxnorm_quant_fwd_ex(FAKE, T, H, p, fmt, FAKE, FAKE, FAKE, variant, None)
+    assert rc == status, L.mxnorm_last_error()
+    if status:
+        assert L.mxnorm_last_error()
+
+
+def test_null_and_misaligned_pointers(L):
+    assert L.mxnorm_quant_fwd(None, 8, 64, 2, 0, FAKE, FAKE, FAKE, None) == 1
+    assert L.mxnorm_quant_fwd(FAKE + 8, 8, 64, 2, 0, FAKE, FAKE, FAKE, None) == 3
+    assert L.mxnorm_quant_fwd(FAKE, 8, 64, 2, 0, FAKE + 4, FAKE, FAKE, None) == 3
+    assert L.mxnorm_quant_fwd(FAKE, 8, 64, 2, 0, FAKE, FAKE, FAKE + 2, None) == 3
+    assert L.rmsnorm_mxfp8_ref_fwd(FAKE, 8, 64, 1e-5, None, FAKE, FAKE, FAKE, None) == 1
+    assert L.rmsnorm_mxfp8_ref_fwd(FAKE, 8, 64, 1e-5, FAKE + 8, FAKE, FAKE, FAKE, None) == 3
+    assert L.rmsnorm_mxfp8_ref_fwd(FAKE, 8, 64, -1.0, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert L.rmsnorm_mxfp8_ref_fwd(FAKE, 0, 64, 1e-5, FAKE, FAKE, FAKE, FAKE, None) == 0
+
+
+def test_python_binding_raises_on_status(L):
+    with pytest.raises(mx.MXNormError) as ei:
+        mx.mxnorm_quant_fwd(FAKE, 8, 48, 2, 0, FAKE, FAKE, FAKE)
+    assert ei.value.status == 1 and "multiple of 32" in str(ei.value)
+
+
+def test_product_path_does_not_import_oracle():
+    """The package (binding, generator, build script) never imports the
+    oracle, and the oracle never imports the package."""
+    pkg = os.path.join(ROOT, "mx_scale_reusing_gb300")
+    for f in os.listdir(pkg):
+        if f.endswith(".py"):
+            assert not re.search(r"^\s*(import|from)\s+oracle", open(os.path.join(pkg, f)).read(), re.M), f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c")):
+            assert "mx_scale_reusing_gb300" not in open(os.path.join(ROOT, "oracle", f)).read(), f
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(mx, "_lib", None)
+    monkeypatch.setattr(mx, "library_path", str(tmp_path / "absent.so"))
+    with pytest.raises(mx.MXNormLibraryMissing):
+        mx.lib()
