@@ -1,14 +1,18 @@
-// mx_row.cuh -- per-lane MX cast of one chunk of a row and the row loop,
-// shared by the warp-row kernel (global loads) and the tiled kernel
-// (shared-memory loads).  Lane layout: lane l of chunk c holds elements
-// [c*32*VEC + l*VEC, +VEC) of the row; an MX block spans 32/VEC lanes.
+// mx_row.cuh -- per-lane MX cast of one chunk of a row, the power-mean
+// finish of a row, and the two row loops built on them: the streaming loop
+// of the warp-row kernel (global loads, rolling prefetch across rows) and
+// the single-row loop of the tiled kernel (shared-memory loads).
+//
+// Lane layout: lane l of chunk c holds elements [c*32*VEC + l*VEC, +VEC) of
+// the row; an MX block spans 32/VEC lanes, whose first lane ("lead") writes
+// the block's E8M0 byte and carries its exponent into the power mean.
 #pragma once
 
 #include "mx_device.cuh"
 
 namespace mxnorm {
 
-// Lane's VEC bf16 values as VEC/2 bf16x2 words.
+// Lane's VEC bf16 values (as VEC/2 bf16x2 words) from global memory.
 template <int VEC, bool LOAD32>
 __device__ __forceinline__ void load_lane(const uint16_t* src, uint32_t (&w)[VEC / 2]) {
   if constexpr (VEC == 8) {
@@ -24,52 +28,69 @@ __device__ __forceinline__ void load_lane(const uint16_t* src, uint32_t (&w)[VEC
   }
 }
 
-// Cast one lane's VEC values of a chunk; returns through `e_out` the block's
-// shared exponent (or kExpNone for a non-finite block).
+// max(|a|, |b|, |c|) propagating NaN (sm_100+ three-input max).
+__device__ __forceinline__ float absmax3(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)), "f"(fabsf(c)));
+  return r;
+}
+
+// max(a, b, c) of non-negative values, propagating NaN.
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float max2_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// max_i |v_i| as a tree of three-input maxima (NaN wins over everything,
+// Inf over every finite value).
+__device__ __forceinline__ float absmax_tree(const float (&v)[16]) {
+  const float a = absmax3(v[0], v[1], v[2]);
+  const float b = absmax3(v[3], v[4], v[5]);
+  const float c = absmax3(v[6], v[7], v[8]);
+  const float d = absmax3(v[9], v[10], v[11]);
+  const float e = absmax3(v[12], v[13], v[14]);
+  return max2_nan(max3_nan(a, b, c), max3_nan(d, e, fabsf(v[15])));
+}
+__device__ __forceinline__ float absmax_tree(const float (&v)[8]) {
+  const float a = absmax3(v[0], v[1], v[2]);
+  const float b = absmax3(v[3], v[4], v[5]);
+  return max3_nan(a, b, max2_nan(fabsf(v[6]), fabsf(v[7])));
+}
+
+// Cast one lane's VEC values of a chunk: block absmax (NaN/Inf-aware),
+// shared exponent, scaled saturating RNE codes, stores of codes and (lead
+// lane) of the scale byte.  Returns the block's exponent, or kExpNone for a
+// block holding Inf/NaN.  Every lane of the warp must call it (shuffles).
 template <int FMT, int VEC>
-__device__ __forceinline__ void cast_lane(const uint32_t (&w)[VEC / 2], bool valid,
-                                          uint8_t* code_dst, uint8_t* scale_dst, bool lead,
-                                          int& e_out) {
+__device__ __forceinline__ int cast_lane(const uint32_t (&w)[VEC / 2], bool valid, uint8_t* code_dst,
+                                         uint8_t* scale_dst, bool lead) {
   using Tr = FmtTraits<FMT>;
   constexpr int LPB = kBlock / VEC;  // lanes per block
   float v[VEC];
-  bool nonfinite;
-  int e;
+#pragma unroll
+  for (int i = 0; i < VEC / 2; ++i) {
+    v[2 * i] = bf16lo(w[i]);
+    v[2 * i + 1] = bf16hi(w[i]);
+  }
   if constexpr (Tr::h16) {
     static_assert(VEC == 16, "H16 needs a whole 16-element group per lane");
-#pragma unroll
-    for (int i = 0; i < VEC / 2; ++i) {
-      v[2 * i] = bf16lo(w[i]);
-      v[2 * i + 1] = bf16hi(w[i]);
-    }
     h16_inplace(v);
-    float a = 0.0f;
-#pragma unroll
-    for (int i = 0; i < VEC; ++i) a = absmax_nan(a, v[i]);
-#pragma unroll
-    for (int off = 1; off < LPB; off <<= 1) {
-      const float o = __shfl_xor_sync(0xFFFFFFFFu, a, off);
-      asm("max.NaN.f32 %0, %0, %1;" : "+f"(a) : "f"(o));
-    }
-    const uint32_t ab = __float_as_uint(a) & 0x7FFFFFFFu;
-    nonfinite = ab >= 0x7F800000u;
-    e = shared_exponent<Tr::emax>((int)(ab >> 23));
-  } else {
-    uint32_t a = 0;
-#pragma unroll
-    for (int i = 0; i < VEC / 2; ++i) a = absmax_bf16x2(a, w[i]);
-    a = max(a & 0xFFFFu, a >> 16);
-#pragma unroll
-    for (int off = 1; off < LPB; off <<= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
-    nonfinite = a >= 0x7F80u;
-    e = shared_exponent<Tr::emax>((int)(a >> 7));
-#pragma unroll
-    for (int i = 0; i < VEC / 2; ++i) {
-      v[2 * i] = bf16lo(w[i]);
-      v[2 * i + 1] = bf16hi(w[i]);
-    }
   }
-  if (nonfinite) e = 0;  // keep the multiply harmless; codes are replaced below
+  float a = absmax_tree(v);
+#pragma unroll
+  for (int off = 1; off < LPB; off <<= 1) {
+    a = max2_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+  }
+  const uint32_t ab = __float_as_uint(a) & 0x7FFFFFFFu;
+  const bool nonfinite = ab >= 0x7F800000u;
+  int e = shared_exponent<Tr::emax>((int)(ab >> 23));
+  if (nonfinite) e = 0;  // keeps the multiply harmless; codes are replaced below
   const float mul = exp2_neg(e);
 #pragma unroll
   for (int i = 0; i < VEC; ++i) v[i] = __fmul_rn(v[i], mul);
@@ -97,15 +118,105 @@ __device__ __forceinline__ void cast_lane(const uint32_t (&w)[VEC / 2], bool val
     }
     if (lead) *scale_dst = nonfinite ? (uint8_t)0xFF : (uint8_t)(e + 127);
   }
-  e_out = nonfinite ? kExpNone : e;
+  return nonfinite ? kExpNone : e;
 }
 
+// Power mean of a row from the exponents each lane collected (ev[c] for its
+// chunks, meaningful where own[c]): m = the row's largest exponent (warp
+// max), then the fixed-point sum sum_k 2^(F + p (e_k - m)) (terms below 2^0
+// dropped: relative error < K 2^-F), then inv_rms in fp64 rounded to fp32.
+// A block marked kExpNone (Inf/NaN) makes the row's inv_rms NaN.
+template <int NCHUNK>
+__device__ __forceinline__ float finish_row(const int (&ev)[NCHUNK], const bool (&own)[NCHUNK], int K, int p) {
+  int mloc = kExpNone;
+  bool bad = false;
+#pragma unroll
+  for (int c = 0; c < NCHUNK; ++c) {
+    if (own[c]) {
+      if (ev[c] == kExpNone) bad = true;
+      else mloc = max(mloc, ev[c]);
+    }
+  }
+  int m = mloc;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  unsigned long long s = 0ull;
+#pragma unroll
+  for (int c = 0; c < NCHUNK; ++c) {
+    const int t = kFixedBits + p * (ev[c] - m);
+    if (own[c] && ev[c] != kExpNone && t >= 0) s += 1ull << t;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+  bad = __any_sync(0xFFFFFFFFu, bad);
+  if (bad) return __uint_as_float(0x7FC00000u);
+  return pm_inv_rms(PowerMeanAcc{m, s}, K, p);
+}
 
-// One row: loads through `load(e0, w)` (e0 = the lane's first element), MX
-// cast of every chunk, stores of codes/scales and, when ESTIMATE, the row's
-// inv_rms from the power mean of its block scales.  NCHUNK > 0 issues all
-// of the row's loads before any arithmetic; NCHUNK == 0 handles any H in
-// batches of four chunks.  Every lane of the warp must call it.
+// Streaming row loop of the warp-row kernel: rows row0, row0 + rstride, ...
+// of x, each NCHUNK chunks of 32*VEC elements.  A ring of AHEAD chunk
+// buffers per lane keeps AHEAD loads in flight: the refill of a buffer is
+// issued (for this row's chunk c + AHEAD, or the next row's first chunks)
+// before the chunk it held is cast.  EXACT: H == NCHUNK * 32 * VEC.
+template <int FMT, int VEC, int NCHUNK, int AHEAD, bool EXACT, bool LOAD32, bool ESTIMATE>
+__device__ __forceinline__ void mx_rows_stream(const uint16_t* __restrict__ x, int64_t T, int H,
+                                               uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                               float* __restrict__ inv_rms, int p, int64_t row,
+                                               int64_t rstride) {
+  static_assert(NCHUNK % AHEAD == 0, "the ring must tile the row");
+  using Tr = FmtTraits<FMT>;
+  constexpr int LPB = kBlock / VEC;
+  constexpr int CE = 32 * VEC;
+  const int Hc = EXACT ? NCHUNK * CE : H;
+  const int lane = threadIdx.x & 31;
+  const bool lead = (lane % LPB) == 0;
+  const int K = Hc / kBlock;
+  const int64_t code_row = Tr::fp4 ? (int64_t)(Hc / 2) : (int64_t)Hc;
+  if (row >= T) return;
+
+  uint32_t buf[AHEAD][VEC / 2];
+  auto issue = [&](int64_t r, int c, uint32_t (&dst)[VEC / 2]) {
+    const int e0 = c * CE + lane * VEC;
+    if (EXACT || e0 < Hc) {
+      load_lane<VEC, LOAD32>(x + r * (int64_t)Hc + e0, dst);
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC / 2; ++i) dst[i] = 0u;
+    }
+  };
+#pragma unroll
+  for (int a = 0; a < AHEAD; ++a) issue(row, a, buf[a]);
+
+  for (; row < T; row += rstride) {
+    const int64_t next = row + rstride;
+    uint8_t* cr = codes + row * code_row;
+    uint8_t* sr = scales + row * (int64_t)K;
+    int ev[NCHUNK];
+    bool own[NCHUNK];
+#pragma unroll
+    for (int c = 0; c < NCHUNK; ++c) {
+      uint32_t w[VEC / 2];
+#pragma unroll
+      for (int i = 0; i < VEC / 2; ++i) w[i] = buf[c % AHEAD][i];
+      const int cc = c + AHEAD;
+      if (cc < NCHUNK) issue(row, cc, buf[c % AHEAD]);
+      else if (next < T) issue(next, cc - NCHUNK, buf[c % AHEAD]);
+      const int e0 = c * CE + lane * VEC;
+      const bool valid = EXACT || e0 < Hc;
+      ev[c] = cast_lane<FMT, VEC>(w, valid, cr + (Tr::fp4 ? e0 / 2 : e0), sr + e0 / kBlock, lead);
+      own[c] = valid && lead;
+    }
+    if constexpr (ESTIMATE) {
+      const float inv = finish_row<NCHUNK>(ev, own, K, p);
+      if (lane == 0) inv_rms[row] = inv;
+    }
+  }
+}
+
+// One row through a loader `load(e0, w)` (e0 = the lane's first element):
+// NCHUNK > 0 issues all of the row's loads before any arithmetic; NCHUNK ==
+// 0 handles any H in batches of four chunks with the running-maximum
+// power-mean accumulator.  Every lane of the warp must call it.
 template <int FMT, int VEC, int NCHUNK, bool ESTIMATE, class Load>
 __device__ __forceinline__ void mx_row(Load load, int H, int p, uint8_t* cr, uint8_t* sr,
                                        float* inv_dst) {
@@ -114,21 +225,7 @@ __device__ __forceinline__ void mx_row(Load load, int H, int p, uint8_t* cr, uin
   constexpr int CE = 32 * VEC;
   const int lane = threadIdx.x & 31;
   const bool lead = (lane % LPB) == 0;
-  PowerMeanAcc acc{kExpNone, 0ull};
-  bool row_nonfinite = false;
-
-  auto do_chunk = [&](int c, const uint32_t (&w)[VEC / 2]) {
-    const int e0 = c * CE + lane * VEC;
-    const bool valid = e0 < H;
-    int e;
-    cast_lane<FMT, VEC>(w, valid, cr + (Tr::fp4 ? e0 / 2 : e0), sr + e0 / kBlock, lead, e);
-    if constexpr (ESTIMATE) {
-      if (valid && lead) {
-        if (e == kExpNone) row_nonfinite = true;
-        else pm_add(acc, e, p);
-      }
-    }
-  };
+  const int K = H / kBlock;
 
   if constexpr (NCHUNK > 0) {
     uint32_t w[NCHUNK][VEC / 2];
@@ -142,9 +239,22 @@ __device__ __forceinline__ void mx_row(Load load, int H, int p, uint8_t* cr, uin
         for (int i = 0; i < VEC / 2; ++i) w[c][i] = 0u;
       }
     }
+    int ev[NCHUNK];
+    bool own[NCHUNK];
 #pragma unroll
-    for (int c = 0; c < NCHUNK; ++c) do_chunk(c, w[c]);
+    for (int c = 0; c < NCHUNK; ++c) {
+      const int e0 = c * CE + lane * VEC;
+      const bool valid = e0 < H;
+      ev[c] = cast_lane<FMT, VEC>(w[c], valid, cr + (Tr::fp4 ? e0 / 2 : e0), sr + e0 / kBlock, lead);
+      own[c] = valid && lead;
+    }
+    if constexpr (ESTIMATE) {
+      const float inv = finish_row<NCHUNK>(ev, own, K, p);
+      if (lane == 0) *inv_dst = inv;
+    }
   } else {
+    PowerMeanAcc acc{kExpNone, 0ull};
+    bool row_nonfinite = false;
     constexpr int BATCH = 4;
     const int nchunk = (H + CE - 1) / CE;
     for (int c0 = 0; c0 < nchunk; c0 += BATCH) {
@@ -160,16 +270,23 @@ __device__ __forceinline__ void mx_row(Load load, int H, int p, uint8_t* cr, uin
         }
       }
 #pragma unroll
-      for (int b = 0; b < BATCH; ++b)
-        if (c0 + b < nchunk) do_chunk(c0 + b, w[b]);
+      for (int b = 0; b < BATCH; ++b) {
+        if (c0 + b < nchunk) {
+          const int e0 = (c0 + b) * CE + lane * VEC;
+          const bool valid = e0 < H;
+          const int e = cast_lane<FMT, VEC>(w[b], valid, cr + (Tr::fp4 ? e0 / 2 : e0), sr + e0 / kBlock, lead);
+          if (ESTIMATE && valid && lead) {
+            if (e == kExpNone) row_nonfinite = true;
+            else pm_add(acc, e, p);
+          }
+        }
+      }
     }
-  }
-
-  if constexpr (ESTIMATE) {
-    const int K = H / kBlock;
-    acc = pm_warp_reduce(acc, p);
-    row_nonfinite = __any_sync(0xFFFFFFFFu, row_nonfinite);
-    if (lane == 0) *inv_dst = row_nonfinite ? __uint_as_float(0x7FC00000u) : pm_inv_rms(acc, K, p);
+    if constexpr (ESTIMATE) {
+      acc = pm_warp_reduce(acc, p);
+      row_nonfinite = __any_sync(0xFFFFFFFFu, row_nonfinite);
+      if (lane == 0) *inv_dst = row_nonfinite ? __uint_as_float(0x7FC00000u) : pm_inv_rms(acc, K, p);
+    }
   }
 }
 

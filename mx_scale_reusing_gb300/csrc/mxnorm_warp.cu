@@ -25,11 +25,23 @@ namespace {
 
 constexpr int kWarpsPerCta = 8;
 
-template <int FMT, int VEC, int NCHUNK, bool LOAD32, bool ESTIMATE>
+// MINB: CTAs per SM the register allocation must allow (occupancy floor).
+template <int FMT, int VEC, int NCHUNK, int AHEAD, bool EXACT, bool LOAD32, bool ESTIMATE, int MINB>
+__global__ void __launch_bounds__(kWarpsPerCta * 32, MINB)
+    mx_warp_row_kernel(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
+                       uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p) {
+  const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+  mx_rows_stream<FMT, VEC, NCHUNK, AHEAD, EXACT, LOAD32, ESTIMATE>(x, T, H, codes, scales, inv_rms, p,
+                                                                   warp0, nwarps);
+}
+
+// Any H (a multiple of 32): batches of four chunks per row.
+template <int FMT, int VEC, bool LOAD32, bool ESTIMATE>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
-    mx_warp_row_kernel(const uint16_t* __restrict__ x, int64_t T, int H,
-                       uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                       float* __restrict__ inv_rms, int p) {
+    mx_warp_row_generic_kernel(const uint16_t* __restrict__ x, int64_t T, int H,
+                               uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                               float* __restrict__ inv_rms, int p) {
   using Tr = FmtTraits<FMT>;
   const int K = H / kBlock;
   const int64_t code_row = Tr::fp4 ? (int64_t)(H / 2) : (int64_t)H;
@@ -38,34 +50,46 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   for (int64_t row = warp0; row < T; row += nwarps) {
     const uint16_t* xr = x + row * (int64_t)H;
     auto load = [xr](int e0, uint32_t (&w)[VEC / 2]) { load_lane<VEC, LOAD32>(xr + e0, w); };
-    mx_row<FMT, VEC, NCHUNK, ESTIMATE>(load, H, p, codes + row * code_row, scales + row * (int64_t)K,
-                                       inv_rms + row);
+    mx_row<FMT, VEC, 0, ESTIMATE>(load, H, p, codes + row * code_row, scales + row * (int64_t)K,
+                                  inv_rms + row);
   }
 }
 
-template <int FMT, int VEC, int NCHUNK, bool LOAD32, bool ESTIMATE>
-cudaError_t launch_one(const WarpRowArgs& a, cudaStream_t stream) {
-  auto kern = mx_warp_row_kernel<FMT, VEC, NCHUNK, LOAD32, ESTIMATE>;
+template <class Kern>
+cudaError_t launch_kernel(Kern kern, const WarpRowArgs& a, cudaStream_t stream) {
   const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kWarpsPerCta * 32,
                                    (a.T + kWarpsPerCta - 1) / kWarpsPerCta);
   kern<<<grid, kWarpsPerCta * 32, 0, stream>>>(static_cast<const uint16_t*>(a.x), a.T, (int)a.H,
-                                               static_cast<uint8_t*>(a.codes), a.scales,
-                                               a.inv_rms, a.p);
+                                               static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms, a.p);
   return cudaGetLastError();
+}
+
+// Ring depth and occupancy floor per (format, lane width, chunks per row).
+template <int FMT, int VEC, int NCHUNK>
+struct StreamTuning {
+  static constexpr int ahead = NCHUNK >= 4 ? 4 : NCHUNK;
+  static constexpr int minb = 2;
+};
+
+template <int FMT, int VEC, int NCHUNK, bool LOAD32, bool ESTIMATE>
+cudaError_t launch_stream(const WarpRowArgs& a, cudaStream_t s) {
+  using Tu = StreamTuning<FMT, VEC, NCHUNK>;
+  if (a.H == (int64_t)NCHUNK * 32 * VEC)
+    return launch_kernel(mx_warp_row_kernel<FMT, VEC, NCHUNK, Tu::ahead, true, LOAD32, ESTIMATE, Tu::minb>, a, s);
+  return launch_kernel(mx_warp_row_kernel<FMT, VEC, NCHUNK, Tu::ahead, false, LOAD32, ESTIMATE, Tu::minb>, a, s);
 }
 
 template <int FMT, int VEC, bool LOAD32, bool ESTIMATE>
 cudaError_t launch_by_h(const WarpRowArgs& a, cudaStream_t s) {
   const int64_t CE = 32 * VEC;
-  const int64_t n = (a.H + CE - 1) / CE;
-  switch (n) {
-    case 1: return launch_one<FMT, VEC, 1, LOAD32, ESTIMATE>(a, s);
-    case 2: return launch_one<FMT, VEC, 2, LOAD32, ESTIMATE>(a, s);
-    case 3: return launch_one<FMT, VEC, 3, LOAD32, ESTIMATE>(a, s);
-    case 4: return launch_one<FMT, VEC, 4, LOAD32, ESTIMATE>(a, s);
-    case 8: return launch_one<FMT, VEC, 8, LOAD32, ESTIMATE>(a, s);
-    case 16: return launch_one<FMT, VEC, 16, LOAD32, ESTIMATE>(a, s);
-    default: return launch_one<FMT, VEC, 0, LOAD32, ESTIMATE>(a, s);
+  switch ((a.H + CE - 1) / CE) {
+    case 1: return launch_stream<FMT, VEC, 1, LOAD32, ESTIMATE>(a, s);
+    case 2: return launch_stream<FMT, VEC, 2, LOAD32, ESTIMATE>(a, s);
+    case 3: return launch_stream<FMT, VEC, 3, LOAD32, ESTIMATE>(a, s);
+    case 4: return launch_stream<FMT, VEC, 4, LOAD32, ESTIMATE>(a, s);
+    case 8: return launch_stream<FMT, VEC, 8, LOAD32, ESTIMATE>(a, s);
+    case 16: return launch_stream<FMT, VEC, 16, LOAD32, ESTIMATE>(a, s);
+    default: return launch_kernel(mx_warp_row_generic_kernel<FMT, VEC, LOAD32, ESTIMATE>, a, s);
   }
 }
 
