@@ -182,7 +182,12 @@ def run_gpu(args):
     torch.cuda.set_device(dev)
     mx.lib()
 
+    import dataclasses
+
+    from mx_scale_reusing_gb300 import shard
     w = synth.WORKLOADS[WORKLOAD]
+    if world > 1:  # weak scaling: every rank streams a full batch of its own rows
+        w = dataclasses.replace(w, seed=shard.rank_seed(w.seed, rank))
     T, H, p = w.T, w.H, 2
     xb = synth.make_activations(w)
     x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16)
@@ -210,10 +215,7 @@ def run_gpu(args):
         dist.barrier()
     ms_step = region / args.steps
     mean_launch = statistics.fmean(per)
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = shard.max_over_ranks(ms_step, dev)
     tokens_per_s = world * T / (ms_step * 1e-3)
 
     peaks, peak_kind = measured_peaks()
@@ -272,10 +274,7 @@ def run_gpu(args):
 
     # ---- e2e through the public API from pinned host buffers
     e2e = run_e2e(torch, mx, x_host, T, H, dev, args.e2e_steps)
-    if world > 1:
-        t = torch.tensor([e2e["ms_per_step"]], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["ms_per_step"] = float(t.item())
+    e2e["ms_per_step"] = shard.max_over_ranks(e2e["ms_per_step"], dev)
     e2e_val = world * T / (e2e["ms_per_step"] * 1e-3)
 
     if rank == 0:
