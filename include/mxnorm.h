@@ -42,9 +42,11 @@
  *            uint8  [T, H/2] (E2M1, E2M1_H16)
  *   scales   uint8  [T, H/32]       any alignment
  *   inv_rms  float  [T]             4-byte aligned
- * The library allocates no device memory, keeps no state between calls
- * except a per-thread error string and a per-device launch-shape cache, and
- * never synchronises: work is queued on `stream` (a cudaStream_t; NULL is
+ * No call allocates device memory (the one buffer the library holds is the
+ * static workspace of rmsnorm_mxfp8_ref_fwd_static_ws, below); the library
+ * keeps no state between calls except a per-thread error string and
+ * per-device launch-shape and workspace-address caches, and it never
+ * synchronises: work is queued on `stream` (a cudaStream_t; NULL is
  * the legacy default stream) and the call returns.  Outputs are fully
  * written when the stream reaches the kernel's end; after an error return
  * they are unspecified.  Inputs and outputs must not overlap.
@@ -114,6 +116,29 @@ int mxnorm_quant_fwd_ex(const void* x, int64_t T, int64_t H, int p, int fmt, voi
  * return.  No gain (gamma = 1). */
 int rmsnorm_mxfp8_ref_fwd(const void* x, int64_t T, int64_t H, float eps, void* y_workspace,
                           uint8_t* codes, uint8_t* scales, float* inv_rms, void* stream);
+
+/* Allocation-free form of rmsnorm_mxfp8_ref_fwd.  The paper has no
+ * counterpart: this exists for callers that cannot allocate device memory
+ * (a host framework that owns every allocation through its own pool, a
+ * latency-critical path that cannot afford cudaMalloc's implicit
+ * synchronisation, a device-memory budget fixed up front).  The bf16
+ * workspace between the two kernels lives in a file-scope device array of
+ * MXNORM_STATIC_WS_BYTES compiled into the library, held by every GPU that
+ * loads it until the process exits; the call itself allocates nothing.
+ *   - T * H must not exceed MXNORM_STATIC_WS_BYTES / 2 (16,777,216 bf16
+ *     elements); larger problems return MXNORM_ERR_UNSUPPORTED.
+ *   - All calls on a device share the array: calls whose work overlaps on
+ *     the GPU (other streams, other host threads) race on it and must be
+ *     serialised by the caller.  The array keeps the last call's y; nothing
+ *     in it needs to start at zero.
+ *   - The first call on each device, with that device current, looks up the
+ *     array's device address once (cudaGetSymbolAddress); make that first
+ *     call before any stream capture.
+ * Arguments, outputs and other errors as rmsnorm_mxfp8_ref_fwd without
+ * y_workspace. */
+#define MXNORM_STATIC_WS_BYTES (32u << 20)
+int rmsnorm_mxfp8_ref_fwd_static_ws(const void* x, int64_t T, int64_t H, float eps, uint8_t* codes,
+                                    uint8_t* scales, float* inv_rms, void* stream);
 
 /* Static text for a status code. */
 const char* mxnorm_status_string(int status);

@@ -54,6 +54,8 @@ int check_common(const void* x, int64_t T, int64_t H, const void* codes, const v
 
 }  // namespace
 
+void set_last_error(const char* msg) { g_last_error = msg; }
+
 int persistent_grid(const void* kernel, int threads, int64_t work_ctas, size_t dyn_smem) {
   int dev = 0;
   cudaGetDevice(&dev);

@@ -43,6 +43,9 @@ cudaError_t launch_rmsnorm_bf16(const RmsNormArgs& a, cudaStream_t s);
 cudaError_t launch_mxnorm_tiled(const TiledArgs& a, cudaStream_t s);
 bool tiled_supported(int64_t H, int fmt);
 
+// Replace the calling thread's message returned by mxnorm_last_error().
+void set_last_error(const char* msg);
+
 // Copy (and optionally zero) the device error word that bounded waits set.
 cudaError_t read_device_error_word(uint32_t* out, bool clear);
 
