@@ -81,21 +81,43 @@ __device__ __forceinline__ void stg4(void* p, uint32_t a) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// ---------------------------------------------------------------- absmax
-// Packed |bf16| maximum on raw bits: for |x| bit patterns the unsigned
-// integer order is the magnitude order, with Inf (0x7F80) and NaN (> 0x7F80)
-// above every finite value, so non-finite blocks show up as amax >= 0x7F80.
-__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
-  return __vmaxu2(acc, w & 0x7FFF7FFFu);
+// ------------------------------------------------------ packed fp32 pairs
+// sm_100+ executes add/sub/mul on two fp32 lanes of a 64-bit register pair
+// per instruction; each half is rounded exactly like the scalar op (.rn,
+// no flush to zero).
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
 }
-
-// max(|a|, b) propagating NaN (b already non-negative).
-__device__ __forceinline__ float absmax_nan(float acc, float v) {
-  float r;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(acc), "f"(fabsf(v)));
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
 
+// v[i] *= s for every element, two per instruction.
+template <int N>
+__device__ __forceinline__ void scale_pairs(float (&v)[N], float s) {
+  const unsigned long long ss = f2_pack(s, s);
+#pragma unroll
+  for (int i = 0; i < N; i += 2) f2_unpack(f2_mul(f2_pack(v[i], v[i + 1]), ss), v[i], v[i + 1]);
+}
+
+// ------------------------------------------------------------ exponents
 // Shared exponent from the biased exponent field of the block absmax:
 // floor(log2 amax) = field - 127 for normal amax; zero and subnormal amax
 // give an exponent below -127 + emax and clamp to -127 (bf16 and fp32 alike).
@@ -138,20 +160,35 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(float v0, float v1, float v2, flo
 // order, butterfly stages h = 1, 2, 4, 8, each add/sub rounded to fp32, then
 // the 1/4 scale ("Entrenamiento Previo ... con MXFP4", Metodologia, item 3:
 // deterministic 16x16 Hadamard rotation before the MXFP4 cast).
+// The stages are evaluated on the pairs q_j = (v_j, v_{j+8}), j = 0..7: for
+// h = 1, 2, 4 a packed add/sub of q_i and q_{i+h} is exactly the scalar
+// butterfly on (v_i, v_{i+h}) and on (v_{i+8}, v_{i+h+8}); stage 8 combines
+// the two halves of each pair.  Every element sees the same fp32 operations
+// in the same stage order as the scalar definition, so results are
+// bit-identical to it.
 __device__ __forceinline__ void h16_inplace(float (&v)[16]) {
+  unsigned long long q[8];
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
+  for (int j = 0; j < 8; ++j) q[j] = f2_pack(v[j], v[j + 8]);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
       if ((i & h) == 0) {
-        const float a = v[i], b = v[i + h];
-        v[i] = __fadd_rn(a, b);
-        v[i + h] = __fsub_rn(a, b);
+        const unsigned long long a = q[i], b = q[i + h];
+        q[i] = f2_add(a, b);
+        q[i + h] = f2_sub(a, b);
       }
     }
   }
+  const unsigned long long quarter = f2_pack(0.25f, 0.25f);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+  for (int j = 0; j < 8; ++j) {
+    float lo, hi;
+    f2_unpack(q[j], lo, hi);
+    const unsigned long long y = f2_pack(__fadd_rn(lo, hi), __fsub_rn(lo, hi));
+    f2_unpack(f2_mul(y, quarter), v[j], v[j + 8]);
+  }
 }
 
 // ------------------------------------------------------------ power mean
@@ -196,12 +233,17 @@ __device__ __forceinline__ PowerMeanAcc pm_warp_reduce(PowerMeanAcc a, int p) {
 }
 
 // inv_rms = 2^-m * (K / S_real)^(1/p) with S_real = S * 2^-F, i.e.
-// 1 / M_p with M_p = ((1/K) sum_k 2^(p e_k))^(1/p); the mean, root and
-// reciprocal are taken in fp64 (IEEE) and rounded once to fp32.
+// 1 / M_p with M_p = ((1/K) sum_k 2^(p e_k))^(1/p).  fp32 throughout: S
+// rounds once to fp32, K * 2^F / S is one IEEE division, the square root
+// (p = 2) is IEEE, and 2^-m scales exactly (m <= 125 for bf16 or rotated
+// fp32 input, so 2^-m and the result stay normal).  Relative error below
+// 2^-22 (two roundings of 2^-24 plus the fixed-point truncation).
 __device__ __forceinline__ float pm_inv_rms(PowerMeanAcc a, int K, int p) {
-  const double mean = ((double)a.s * 0x1p-48) / (double)K;
-  const double mp = (p == 1) ? mean : sqrt(mean);
-  return (float)scalbn(1.0 / mp, -a.m);
+  const float s = __ull2float_rn(a.s);
+  const float kf = __uint_as_float((uint32_t)(127 + kFixedBits) << 23) * (float)K;  // K * 2^F, exact
+  float q = __fdiv_rn(kf, s);
+  if (p == 2) q = __fsqrt_rn(q);
+  return __fmul_rn(q, exp2_neg(a.m));
 }
 
 }  // namespace mxnorm

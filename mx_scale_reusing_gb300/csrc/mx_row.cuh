@@ -91,9 +91,7 @@ __device__ __forceinline__ int cast_lane(const uint32_t (&w)[VEC / 2], bool vali
   const bool nonfinite = ab >= 0x7F800000u;
   int e = shared_exponent<Tr::emax>((int)(ab >> 23));
   if (nonfinite) e = 0;  // keeps the multiply harmless; codes are replaced below
-  const float mul = exp2_neg(e);
-#pragma unroll
-  for (int i = 0; i < VEC; ++i) v[i] = __fmul_rn(v[i], mul);
+  scale_pairs(v, exp2_neg(e));
 
   if (valid) {
     if constexpr (!Tr::fp4) {
@@ -124,7 +122,7 @@ __device__ __forceinline__ int cast_lane(const uint32_t (&w)[VEC / 2], bool vali
 // Power mean of a row from the exponents each lane collected (ev[c] for its
 // chunks, meaningful where own[c]): m = the row's largest exponent (warp
 // max), then the fixed-point sum sum_k 2^(F + p (e_k - m)) (terms below 2^0
-// dropped: relative error < K 2^-F), then inv_rms in fp64 rounded to fp32.
+// dropped: relative error < K 2^-F), then inv_rms in fp32 (pm_inv_rms).
 // A block marked kExpNone (Inf/NaN) makes the row's inv_rms NaN.
 template <int NCHUNK>
 __device__ __forceinline__ float finish_row(const int (&ev)[NCHUNK], const bool (&own)[NCHUNK], int K, int p) {

@@ -64,11 +64,18 @@ cudaError_t launch_kernel(Kern kern, const WarpRowArgs& a, cudaStream_t stream) 
   return cudaGetLastError();
 }
 
-// Ring depth and occupancy floor per (format, lane width, chunks per row).
+// Ring depth (chunks in flight per warp) and occupancy floor (CTAs of 8
+// warps per SM the register budget must allow), per (format, lane width,
+// chunks per row).  Chosen by interleaved timing of every candidate on
+// 512 MiB inputs on GB300: FP8 rows with 32-byte lanes run best at depth 1
+// with 3 CTAs/SM (80 registers; 64 registers lose ILP), FP4 rows (the H16
+// rotation makes them ALU-heavier) at depth 2 with 4 CTAs/SM, and short rows
+// of 16-byte lanes with the whole row in flight.
 template <int FMT, int VEC, int NCHUNK>
 struct StreamTuning {
-  static constexpr int ahead = NCHUNK >= 4 ? 4 : NCHUNK;
-  static constexpr int minb = 2;
+  static constexpr bool fp4 = FmtTraits<FMT>::fp4;
+  static constexpr int ahead = (VEC == 8) ? NCHUNK : (fp4 && NCHUNK % 2 == 0) ? 2 : (NCHUNK == 2 ? 2 : 1);
+  static constexpr int minb = (VEC == 8 && NCHUNK == 1) ? 8 : (!fp4 && NCHUNK >= 8) ? 3 : 4;
 };
 
 template <int FMT, int VEC, int NCHUNK, bool LOAD32, bool ESTIMATE>

@@ -10,7 +10,8 @@
 // One warp per row, the same lane layout as the MXNorm warp-row kernel.
 // The sum of squares is fp32: a VEC-wide pairwise sum per chunk, a serial
 // sum over chunks and a 5-level warp tree, so its relative error is at most
-// (log2 VEC + chunks + 5) * 2^-24; the root and reciprocal are fp64.
+// (log2 VEC + chunks + 5) * 2^-24; the mean, + eps and the correctly
+// rounded reciprocal square root are fp32 (three more roundings).
 #include "launch.h"
 #include "mx_device.cuh"
 
@@ -68,7 +69,7 @@ __device__ __forceinline__ void store_y(uint16_t* dst, const uint32_t (&w)[VEC /
 __device__ __forceinline__ float finish_inv(float ss, int H, float eps) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, off));
-  return (float)(1.0 / sqrt((double)ss / (double)H + (double)eps));
+  return __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps));
 }
 
 // NCHUNK > 0: the row stays in registers between the two phases.
