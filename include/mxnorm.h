@@ -35,8 +35,10 @@
  * A block holding Inf or NaN gets scale 0xFF (E8M0 NaN), codes 0x7F (E4M3)
  * or 0 (E2M1), and its row's inv_rms is NaN.
  *
- * Memory and ownership.  Every pointer is a DEVICE pointer owned by the
- * caller; row-major, densely packed (row stride = row length):
+ * Memory and ownership.  Every pointer is a device-accessible pointer owned
+ * by the caller: device memory, or pinned host memory mapped into the
+ * device's address space (the kernel then reads and writes it across the
+ * host link).  Row-major, densely packed (row stride = row length):
  *   x        bf16   [T, H]          16-byte aligned
  *   codes    uint8  [T, H]  (E4M3)  16-byte aligned
  *            uint8  [T, H/2] (E2M1, E2M1_H16)

@@ -148,15 +148,20 @@ _host_ws = {}
 
 
 def quant_fwd_host(x, p: int = 2, fmt: str = "mxfp8", out=None, device=None, chunks: int = 8,
-                   variant: str = "auto"):
-    """MXNorm forward of a bf16 CPU tensor (pinned for full copy speed).
+                   variant: str = "auto", mode: str = "auto"):
+    """MXNorm forward of a bf16 CPU tensor; returns (codes, scales, inv_rms)
+    CPU tensors, valid once the current stream of `device` has synchronised.
 
-    The rows are split into `chunks` pieces over three CUDA streams: per
-    piece a host->device copy of x, the C-ABI call, and device->host copies
-    of codes, scales and inv_rms, so copies in both directions overlap with
-    each other and with the kernels.  Device staging buffers are cached per
-    (device, shape, fmt).  Returns (codes, scales, inv_rms) CPU tensors,
-    valid once the current stream of `device` has synchronised.
+    mode "zero_copy": x and the outputs are pinned host memory, which is
+    mapped into the GPU's address space; the kernel reads x and writes its
+    outputs across the host link directly (no staging buffers, no copy
+    engine).  On Grace-Blackwell this runs at the host link's speed.
+    mode "staged": the rows are split into `chunks` pieces over three CUDA
+    streams: per piece a host->device copy of x, the C-ABI call, and
+    device->host copies of codes, scales and inv_rms, so copies in both
+    directions overlap with each other and with the kernels; device
+    staging buffers are cached per (device, shape, fmt).
+    mode "auto": zero_copy when x and every output are pinned, else staged.
     """
     import torch
     if x.is_cuda or x.dtype != torch.bfloat16 or not x.is_contiguous():
@@ -171,6 +176,19 @@ def quant_fwd_host(x, p: int = 2, fmt: str = "mxfp8", out=None, device=None, chu
         out = (torch.empty((T, cb), dtype=torch.uint8).pin_memory(),
                torch.empty((T, H // 32), dtype=torch.uint8).pin_memory(),
                torch.empty((T,), dtype=torch.float32).pin_memory())
+    pinned = x.is_pinned() and all(t.is_pinned() and t.is_contiguous() for t in out)
+    if mode == "auto":
+        mode = "zero_copy" if pinned else "staged"
+    if mode == "zero_copy":
+        if not pinned:
+            raise ValueError("zero_copy needs x and every output in pinned (page-locked) host memory")
+        with torch.cuda.device(device):
+            _check(lib().mxnorm_quant_fwd_ex(x.data_ptr(), T, H, int(p), FMT[fmt], out[0].data_ptr(),
+                                             out[1].data_ptr(), out[2].data_ptr(), VARIANT[variant],
+                                             _stream_ptr(device, None)))
+        return out
+    if mode != "staged":
+        raise ValueError(f"unknown mode {mode!r}")
     oc, os_, oi = (t.view(-1) for t in out)
     key = (device.index, T, H, fmt)
     ws = _host_ws.get(key)

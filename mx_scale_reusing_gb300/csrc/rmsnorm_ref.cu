@@ -74,8 +74,9 @@ __device__ __forceinline__ float finish_inv(float ss, int H, float eps) {
 
 // NCHUNK > 0: the row stays in registers between the two phases.
 // NCHUNK == 0: any H; the second phase re-reads the row (L1/L2 hits).
+// Two CTAs per SM (128 registers) time best for the register-resident row.
 template <int VEC, int NCHUNK>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 2)
     rmsnorm_bf16_kernel(const uint16_t* __restrict__ x, int64_t T, int H, float eps,
                         uint16_t* __restrict__ y, float* __restrict__ inv_rms) {
   constexpr int CE = 32 * VEC;

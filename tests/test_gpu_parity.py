@@ -315,14 +315,15 @@ def test_rmsnorm_baseline_ragged(T, H):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-def test_host_buffer_path(fmt):
-    """quant_fwd_host (pinned host in, pinned host out, chunked over three
-    streams) gives the same bytes as the device path and the oracle."""
+@pytest.mark.parametrize("mode,chunks", [("staged", 1), ("staged", 3), ("staged", 8), ("zero_copy", 1)])
+def test_host_buffer_path(fmt, mode, chunks):
+    """quant_fwd_host (pinned host in, pinned host out; staged over three
+    streams, or zero-copy with the kernel on the pinned buffers) gives the
+    same bytes as the oracle."""
     xb = synth.make_random_rows(1000, 768, seed=21, scale=2.0)
     x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
-    for chunks in (1, 3, 8):
-        c, s, i = mx.quant_fwd_host(x, p=2, fmt=fmt, chunks=chunks)
-        torch.cuda.synchronize()
-        oc, os_, oi = oracle.mxnorm_quant(xb, 2, fmt)
-        assert np.array_equal(c.numpy(), oc) and np.array_equal(s.numpy(), os_)
-        assert_inv_close(i.numpy(), oi)
+    c, s, i = mx.quant_fwd_host(x, p=2, fmt=fmt, chunks=chunks, mode=mode)
+    torch.cuda.synchronize()
+    oc, os_, oi = oracle.mxnorm_quant(xb, 2, fmt)
+    assert np.array_equal(c.numpy(), oc) and np.array_equal(s.numpy(), os_)
+    assert_inv_close(i.numpy(), oi)
