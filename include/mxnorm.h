@@ -19,9 +19,11 @@
  * (gist.science summary), Metodologia, item 3.
  *
  * What one call computes, per row of x (bf16, H elements, H % 32 == 0):
- *   v      = x, or for MXFP4_E2M1_H16 the rotation (1/4) H16 applied to each
- *            aligned group of 16 elements in fp32 (Sylvester order, butterfly
- *            stages 1, 2, 4, 8, each add rounded to fp32, then * 1/4);
+ *   v      = x, or for the *_H16 formats the rotation (1/4) H16 applied to
+ *            each aligned group of 16 elements in fp32 (Sylvester order,
+ *            butterfly stages 1, 2, 4, 8, each add rounded to fp32, then
+ *            * 1/4), or for the *_H32 formats H32 / sqrt(32) on each block
+ *            (stages 1 .. 16, then * RN_fp32(1/sqrt(32)) = 0x3E3504F3);
  *   a_k    = max |v_j| over block k (32 elements), k = 0..K-1;
  *   e_k    = max(floor(log2 a_k) - emax, -127), emax = 8 (E4M3) or 2 (E2M1),
  *            e_k = -127 when a_k = 0;  scales[k] = e_k + 127 (E8M0);
@@ -40,8 +42,8 @@
  * device's address space (the kernel then reads and writes it across the
  * host link).  Row-major, densely packed (row stride = row length):
  *   x        bf16   [T, H]          16-byte aligned
- *   codes    uint8  [T, H]  (E4M3)  16-byte aligned
- *            uint8  [T, H/2] (E2M1, E2M1_H16)
+ *   codes    uint8  [T, H]  (E4M3 formats)  16-byte aligned
+ *            uint8  [T, H/2] (E2M1 formats)
  *   scales   uint8  [T, H/32]       any alignment
  *   inv_rms  float  [T]             4-byte aligned
  * No call allocates device memory (the one buffer the library holds is the
@@ -77,9 +79,12 @@ extern "C" {
 #define MXNORM_ABI_VERSION 1
 
 typedef enum {
-  MXNORM_FMT_MXFP8_E4M3 = 0,     /* FP8 E4M3 codes, one byte per element     */
-  MXNORM_FMT_MXFP4_E2M1 = 1,     /* FP4 E2M1 codes, two per byte             */
-  MXNORM_FMT_MXFP4_E2M1_H16 = 2  /* (1/4) H16 rotation, then FP4 E2M1 codes  */
+  MXNORM_FMT_MXFP8_E4M3 = 0,      /* FP8 E4M3 codes, one byte per element            */
+  MXNORM_FMT_MXFP4_E2M1 = 1,      /* FP4 E2M1 codes, two per byte                    */
+  MXNORM_FMT_MXFP4_E2M1_H16 = 2,  /* (1/4) H16 rotation, then FP4 E2M1 codes         */
+  MXNORM_FMT_MXFP8_E4M3_H16 = 3,  /* (1/4) H16 rotation, then FP8 E4M3 codes         */
+  MXNORM_FMT_MXFP4_E2M1_H32 = 4,  /* H32/sqrt(32) rotation, then FP4 E2M1 codes      */
+  MXNORM_FMT_MXFP8_E4M3_H32 = 5   /* H32/sqrt(32) rotation, then FP8 E4M3 codes      */
 } mxnorm_fmt;
 
 typedef enum {

@@ -22,7 +22,7 @@ __all__ = [
     "code_bytes",
 ]
 
-FMT = {"mxfp8": 0, "mxfp4": 1, "mxfp4_h16": 2}
+FMT = {"mxfp8": 0, "mxfp4": 1, "mxfp4_h16": 2, "mxfp8_h16": 3, "mxfp4_h32": 4, "mxfp8_h32": 5}
 VARIANT = {"auto": 0, "warp_row": 1, "tiled_tma": 2}
 STATUS = {0: "MXNORM_OK", 1: "MXNORM_ERR_INVALID_ARG", 2: "MXNORM_ERR_UNSUPPORTED",
           3: "MXNORM_ERR_MISALIGNED", 4: "MXNORM_ERR_CUDA"}
@@ -75,7 +75,7 @@ def _check(status: int):
 
 
 def code_bytes(H: int, fmt: str) -> int:
-    return H if FMT[fmt] == 0 else H // 2
+    return H if fmt.startswith("mxfp8") else H // 2
 
 
 def _stream_ptr(device, stream):

@@ -88,8 +88,7 @@ int mxnorm_quant_fwd_ex(const void* x, int64_t T, int64_t H, int p, int fmt, voi
                         uint8_t* scales, float* inv_rms, int variant, void* stream) {
   g_last_error.clear();
   if (p != 1 && p != 2) return fail(MXNORM_ERR_INVALID_ARG, "p = %d is not 1 or 2", p);
-  if (fmt != MXNORM_FMT_MXFP8_E4M3 && fmt != MXNORM_FMT_MXFP4_E2M1 && fmt != MXNORM_FMT_MXFP4_E2M1_H16)
-    return fail(MXNORM_ERR_INVALID_ARG, "unknown fmt %d", fmt);
+  if (fmt < 0 || fmt >= kNumFmts) return fail(MXNORM_ERR_INVALID_ARG, "unknown fmt %d", fmt);
   if (variant < MXNORM_VARIANT_AUTO || variant > MXNORM_VARIANT_TILED_TMA)
     return fail(MXNORM_ERR_INVALID_ARG, "unknown variant %d", variant);
   int st = check_common(x, T, H, codes, scales, inv_rms);

@@ -25,27 +25,22 @@ constexpr int kFixedBits = 48;           // F: fixed-point fraction bits of the 
 constexpr int kMaxH = 1 << 20;           // K <= 2^15 keeps K * 2^F below 2^64
 constexpr int kExpNone = -1000;          // "no block seen yet" for the running maximum
 
-enum Fmt : int { kFmtE4M3 = 0, kFmtE2M1 = 1, kFmtE2M1H16 = 2 };
+enum Fmt : int {
+  kFmtE4M3 = 0,      // MXFP8 E4M3
+  kFmtE2M1 = 1,      // MXFP4 E2M1
+  kFmtE2M1H16 = 2,   // (1/4) H16 rotation, then MXFP4
+  kFmtE4M3H16 = 3,   // (1/4) H16 rotation, then MXFP8
+  kFmtE2M1H32 = 4,   // H32 / sqrt(32) rotation, then MXFP4
+  kFmtE4M3H32 = 5,   // H32 / sqrt(32) rotation, then MXFP8
+};
+constexpr int kNumFmts = 6;
 
 template <int FMT>
-struct FmtTraits;
-template <>
-struct FmtTraits<kFmtE4M3> {
-  static constexpr int emax = 8;
-  static constexpr bool fp4 = false;
-  static constexpr bool h16 = false;
-};
-template <>
-struct FmtTraits<kFmtE2M1> {
-  static constexpr int emax = 2;
-  static constexpr bool fp4 = true;
-  static constexpr bool h16 = false;
-};
-template <>
-struct FmtTraits<kFmtE2M1H16> {
-  static constexpr int emax = 2;
-  static constexpr bool fp4 = true;
-  static constexpr bool h16 = true;
+struct FmtTraits {
+  static constexpr bool fp4 = FMT == kFmtE2M1 || FMT == kFmtE2M1H16 || FMT == kFmtE2M1H32;
+  static constexpr int emax = fp4 ? 2 : 8;  // largest element exponent: 6 = 1.5*2^2, 448 = 1.75*2^8
+  static constexpr int rot = (FMT == kFmtE2M1H16 || FMT == kFmtE4M3H16) ? 16
+                             : (FMT == kFmtE2M1H32 || FMT == kFmtE4M3H32) ? 32 : 0;
 };
 
 // ------------------------------------------------------------------ loads
@@ -188,6 +183,36 @@ __device__ __forceinline__ void h16_inplace(float (&v)[16]) {
     f2_unpack(q[j], lo, hi);
     const unsigned long long y = f2_pack(__fadd_rn(lo, hi), __fsub_rn(lo, hi));
     f2_unpack(f2_mul(y, quarter), v[j], v[j + 8]);
+  }
+}
+
+// y = H32 v / sqrt(32) in place for 32 fp32 values: butterfly stages
+// h = 1, 2, 4, 8, 16 in fp32, then each value times RN_fp32(1/sqrt(32)).
+// Same pairing idea as h16_inplace with q_j = (v_j, v_{j+16}): stages 1..8
+// packed, stage 16 across the halves; bit-identical to the scalar order.
+__device__ __forceinline__ void h32_inplace(float (&v)[32]) {
+  unsigned long long q[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) q[j] = f2_pack(v[j], v[j + 16]);
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const unsigned long long a = q[i], b = q[i + h];
+        q[i] = f2_add(a, b);
+        q[i + h] = f2_sub(a, b);
+      }
+    }
+  }
+  const float c32 = 0.17677669f;  // RN_fp32(1/sqrt(32)) = 0x3E3504F3
+  const unsigned long long cc = f2_pack(c32, c32);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float lo, hi;
+    f2_unpack(q[j], lo, hi);
+    const unsigned long long y = f2_pack(__fadd_rn(lo, hi), __fsub_rn(lo, hi));
+    f2_unpack(f2_mul(y, cc), v[j], v[j + 16]);
   }
 }
 

@@ -18,6 +18,19 @@ __device__ __forceinline__ void load_lane(const uint16_t* src, uint32_t (&w)[VEC
   if constexpr (VEC == 8) {
     const uint4 v = ldg_stream16(src);
     w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if constexpr (VEC == 32) {
+    uint32_t (&lo)[8] = *reinterpret_cast<uint32_t(*)[8]>(&w[0]);
+    uint32_t (&hi)[8] = *reinterpret_cast<uint32_t(*)[8]>(&w[8]);
+    if constexpr (LOAD32) {
+      ldg_stream32(src, lo);
+      ldg_stream32(src + 16, hi);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 a = ldg_stream16(src + 8 * q);
+        w[4 * q] = a.x; w[4 * q + 1] = a.y; w[4 * q + 2] = a.z; w[4 * q + 3] = a.w;
+      }
+    }
   } else if constexpr (LOAD32) {
     ldg_stream32(src, w);
   } else {
@@ -57,6 +70,11 @@ __device__ __forceinline__ float absmax_tree(const float (&v)[16]) {
   const float e = absmax3(v[12], v[13], v[14]);
   return max2_nan(max3_nan(a, b, c), max3_nan(d, e, fabsf(v[15])));
 }
+__device__ __forceinline__ float absmax_tree(const float (&v)[32]) {
+  const float (&lo)[16] = *reinterpret_cast<const float(*)[16]>(&v[0]);
+  const float (&hi)[16] = *reinterpret_cast<const float(*)[16]>(&v[16]);
+  return max2_nan(absmax_tree(lo), absmax_tree(hi));
+}
 __device__ __forceinline__ float absmax_tree(const float (&v)[8]) {
   const float a = absmax3(v[0], v[1], v[2]);
   const float b = absmax3(v[3], v[4], v[5]);
@@ -78,9 +96,13 @@ __device__ __forceinline__ int cast_lane(const uint32_t (&w)[VEC / 2], bool vali
     v[2 * i] = bf16lo(w[i]);
     v[2 * i + 1] = bf16hi(w[i]);
   }
-  if constexpr (Tr::h16) {
-    static_assert(VEC == 16, "H16 needs a whole 16-element group per lane");
-    h16_inplace(v);
+  if constexpr (Tr::rot == 16) {
+    static_assert(VEC % 16 == 0, "H16 needs whole 16-element groups per lane");
+#pragma unroll
+    for (int g = 0; g < VEC; g += 16) h16_inplace(*reinterpret_cast<float(*)[16]>(&v[g]));
+  } else if constexpr (Tr::rot == 32) {
+    static_assert(VEC == 32, "H32 needs a whole 32-element block per lane");
+    h32_inplace(*reinterpret_cast<float(*)[32]>(&v[0]));
   }
   float a = absmax_tree(v);
 #pragma unroll
@@ -101,8 +123,14 @@ __device__ __forceinline__ int cast_lane(const uint32_t (&w)[VEC / 2], bool vali
         q[i] = cvt_e4m3x4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         if (nonfinite) q[i] = 0x7F7F7F7Fu;
       }
-      if constexpr (VEC == 16) stg16(code_dst, q[0], q[1], q[2], q[3]);
-      else stg8(code_dst, q[0], q[1]);
+      if constexpr (VEC == 32) {
+        stg16(code_dst, q[0], q[1], q[2], q[3]);
+        stg16(code_dst + 16, q[4], q[5], q[6], q[7]);
+      } else if constexpr (VEC == 16) {
+        stg16(code_dst, q[0], q[1], q[2], q[3]);
+      } else {
+        stg8(code_dst, q[0], q[1]);
+      }
     } else {
       uint32_t q[VEC / 8];
 #pragma unroll
@@ -111,7 +139,8 @@ __device__ __forceinline__ int cast_lane(const uint32_t (&w)[VEC / 2], bool vali
                           v[8 * i + 5], v[8 * i + 6], v[8 * i + 7]);
         if (nonfinite) q[i] = 0u;
       }
-      if constexpr (VEC == 16) stg8(code_dst, q[0], q[1]);
+      if constexpr (VEC == 32) stg16(code_dst, q[0], q[1], q[2], q[3]);
+      else if constexpr (VEC == 16) stg8(code_dst, q[0], q[1]);
       else stg4(code_dst, q[0]);
     }
     if (lead) *scale_dst = nonfinite ? (uint8_t)0xFF : (uint8_t)(e + 127);

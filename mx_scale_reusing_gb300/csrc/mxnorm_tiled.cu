@@ -100,13 +100,11 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
 
 template <int VEC>
 __device__ __forceinline__ void lds_lane(uint32_t saddr, uint32_t (&w)[VEC / 2]) {
-  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-               : "r"(saddr));
-  if constexpr (VEC == 16) {
+#pragma unroll
+  for (int q = 0; q < VEC / 8; ++q) {
     asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-                 : "r"(saddr + 16));
+                 : "=r"(w[4 * q]), "=r"(w[4 * q + 1]), "=r"(w[4 * q + 2]), "=r"(w[4 * q + 3])
+                 : "r"(saddr + 16u * q));
   }
 }
 
@@ -223,9 +221,14 @@ cudaError_t launch_by_h(const TiledArgs& t, cudaStream_t s) {
 
 template <int FMT>
 cudaError_t launch_fmt(const TiledArgs& t, cudaStream_t s) {
-  if (FmtTraits<FMT>::h16 || t.base.H % 512 == 0) return launch_by_h<FMT, 16>(t, s);
-  if constexpr (!FmtTraits<FMT>::h16) return launch_by_h<FMT, 8>(t, s);
-  return cudaErrorInvalidValue;
+  constexpr int rot = FmtTraits<FMT>::rot;
+  if constexpr (rot == 32) {
+    return launch_by_h<FMT, 32>(t, s);
+  } else {
+    if (rot == 16 || t.base.H % 512 == 0) return launch_by_h<FMT, 16>(t, s);
+    if constexpr (rot == 0) return launch_by_h<FMT, 8>(t, s);
+    return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -252,6 +255,9 @@ cudaError_t launch_mxnorm_tiled(const TiledArgs& t, cudaStream_t s) {
     case kFmtE4M3: return launch_fmt<kFmtE4M3>(t, s);
     case kFmtE2M1: return launch_fmt<kFmtE2M1>(t, s);
     case kFmtE2M1H16: return launch_fmt<kFmtE2M1H16>(t, s);
+    case kFmtE4M3H16: return launch_fmt<kFmtE4M3H16>(t, s);
+    case kFmtE2M1H32: return launch_fmt<kFmtE2M1H32>(t, s);
+    case kFmtE4M3H32: return launch_fmt<kFmtE4M3H32>(t, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,137 +1,23 @@
-// mxnorm_warp.cu -- one-row-per-warp MXNorm kernel (and the cast-only form
-// used by the two-pass baseline's second kernel).
-//
-// Work split: each warp owns whole rows (grid-stride over T).  A row is
-// walked in chunks of 32 * VEC elements; lane l of chunk c holds elements
-// [c*32*VEC + l*VEC, +VEC) -- one 16-byte (VEC = 8) or 32-byte (VEC = 16)
-// coalesced load, so a warp reads 512 B or 1 KiB contiguous per chunk.  An
-// MX block (32 elements) is 32/VEC lanes, its absmax a 1-2 step xor
-// shuffle.  With the chunk count known at compile time every load of a row
-// is issued before any arithmetic, which keeps up to 8 KiB per warp in
-// flight.  Per block the lead lane writes the E8M0 byte and feeds the
-// power-mean accumulator; the row's accumulators meet in a warp reduction
-// and lane 0 writes inv_rms.
-//
-// Method: "MXNorm: Reusing MXFP block scales for efficient tensor
-// normalisation", Resumen tecnico, 2. Metodologia: "Fundamentos Teoricos"
-// (rho~ = c(p,B) ((1/K) sum_k m~_k^p)^(-1/p), read with m~_k = s_k, c = 1)
-// and "Implementacion" (the block maxima of the cast feed the estimate in
-// one pass); OCP MX v1.0 6.3 for the cast.
-#include "launch.h"
-#include "mx_row.cuh"
+// mxnorm_warp.cu -- dispatch of the warp-row MXNorm kernel by format
+// family (kernel templates in mx_warp.cuh).
+#include "mx_warp.cuh"
 
 namespace mxnorm {
-namespace {
-
-constexpr int kWarpsPerCta = 8;
-
-// MINB: CTAs per SM the register allocation must allow (occupancy floor).
-template <int FMT, int VEC, int NCHUNK, int AHEAD, bool EXACT, bool LOAD32, bool ESTIMATE, int MINB>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, MINB)
-    mx_warp_row_kernel(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
-                       uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p) {
-  const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-  const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
-  mx_rows_stream<FMT, VEC, NCHUNK, AHEAD, EXACT, LOAD32, ESTIMATE>(x, T, H, codes, scales, inv_rms, p,
-                                                                   warp0, nwarps);
-}
-
-// Any H (a multiple of 32): batches of four chunks per row.
-template <int FMT, int VEC, bool LOAD32, bool ESTIMATE>
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
-    mx_warp_row_generic_kernel(const uint16_t* __restrict__ x, int64_t T, int H,
-                               uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                               float* __restrict__ inv_rms, int p) {
-  using Tr = FmtTraits<FMT>;
-  const int K = H / kBlock;
-  const int64_t code_row = Tr::fp4 ? (int64_t)(H / 2) : (int64_t)H;
-  const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-  const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
-  for (int64_t row = warp0; row < T; row += nwarps) {
-    const uint16_t* xr = x + row * (int64_t)H;
-    auto load = [xr](int e0, uint32_t (&w)[VEC / 2]) { load_lane<VEC, LOAD32>(xr + e0, w); };
-    mx_row<FMT, VEC, 0, ESTIMATE>(load, H, p, codes + row * code_row, scales + row * (int64_t)K,
-                                  inv_rms + row);
-  }
-}
-
-template <class Kern>
-cudaError_t launch_kernel(Kern kern, const WarpRowArgs& a, cudaStream_t stream) {
-  const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kWarpsPerCta * 32,
-                                   (a.T + kWarpsPerCta - 1) / kWarpsPerCta);
-  kern<<<grid, kWarpsPerCta * 32, 0, stream>>>(static_cast<const uint16_t*>(a.x), a.T, (int)a.H,
-                                               static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms, a.p);
-  return cudaGetLastError();
-}
-
-// Ring depth (chunks in flight per warp) and occupancy floor (CTAs of 8
-// warps per SM the register budget must allow), per (format, lane width,
-// chunks per row).  Chosen by interleaved timing of every candidate on
-// 512 MiB inputs on GB300: FP8 rows with 32-byte lanes run best at depth 1
-// with 3 CTAs/SM (80 registers; 64 registers lose ILP), FP4 rows (the H16
-// rotation makes them ALU-heavier) at depth 2 with 4 CTAs/SM, and short rows
-// of 16-byte lanes with the whole row in flight.
-template <int FMT, int VEC, int NCHUNK>
-struct StreamTuning {
-  static constexpr bool fp4 = FmtTraits<FMT>::fp4;
-  static constexpr int ahead = (VEC == 8) ? NCHUNK : (fp4 && NCHUNK % 2 == 0) ? 2 : (NCHUNK == 2 ? 2 : 1);
-  static constexpr int minb = (VEC == 8 && NCHUNK == 1) ? 8 : (!fp4 && NCHUNK >= 8) ? 3 : 4;
-};
-
-template <int FMT, int VEC, int NCHUNK, bool LOAD32, bool ESTIMATE>
-cudaError_t launch_stream(const WarpRowArgs& a, cudaStream_t s) {
-  using Tu = StreamTuning<FMT, VEC, NCHUNK>;
-  if (a.H == (int64_t)NCHUNK * 32 * VEC)
-    return launch_kernel(mx_warp_row_kernel<FMT, VEC, NCHUNK, Tu::ahead, true, LOAD32, ESTIMATE, Tu::minb>, a, s);
-  return launch_kernel(mx_warp_row_kernel<FMT, VEC, NCHUNK, Tu::ahead, false, LOAD32, ESTIMATE, Tu::minb>, a, s);
-}
-
-template <int FMT, int VEC, bool LOAD32, bool ESTIMATE>
-cudaError_t launch_by_h(const WarpRowArgs& a, cudaStream_t s) {
-  const int64_t CE = 32 * VEC;
-  switch ((a.H + CE - 1) / CE) {
-    case 1: return launch_stream<FMT, VEC, 1, LOAD32, ESTIMATE>(a, s);
-    case 2: return launch_stream<FMT, VEC, 2, LOAD32, ESTIMATE>(a, s);
-    case 3: return launch_stream<FMT, VEC, 3, LOAD32, ESTIMATE>(a, s);
-    case 4: return launch_stream<FMT, VEC, 4, LOAD32, ESTIMATE>(a, s);
-    case 8: return launch_stream<FMT, VEC, 8, LOAD32, ESTIMATE>(a, s);
-    case 16: return launch_stream<FMT, VEC, 16, LOAD32, ESTIMATE>(a, s);
-    default: return launch_kernel(mx_warp_row_generic_kernel<FMT, VEC, LOAD32, ESTIMATE>, a, s);
-  }
-}
-
-template <int FMT, bool ESTIMATE>
-cudaError_t launch_fmt(const WarpRowArgs& a, cudaStream_t s) {
-  const bool x32 = (reinterpret_cast<uintptr_t>(a.x) & 31) == 0;
-  // 32-byte lanes when a chunk of 512 elements tiles the row (or when the
-  // H16 rotation needs a whole 16-group per lane), else 16-byte lanes.
-  const bool vec16 = FmtTraits<FMT>::h16 || (a.H % 512 == 0);
-  if (vec16) {
-    if (x32) return launch_by_h<FMT, 16, true, ESTIMATE>(a, s);
-    return launch_by_h<FMT, 16, false, ESTIMATE>(a, s);
-  }
-  if constexpr (!FmtTraits<FMT>::h16) return launch_by_h<FMT, 8, false, ESTIMATE>(a, s);
-  return cudaErrorInvalidValue;
-}
-
-}  // namespace
 
 cudaError_t launch_mxnorm_warp_row(const WarpRowArgs& a, cudaStream_t s) {
   switch (a.fmt) {
-    case kFmtE4M3: return launch_fmt<kFmtE4M3, true>(a, s);
-    case kFmtE2M1: return launch_fmt<kFmtE2M1, true>(a, s);
-    case kFmtE2M1H16: return launch_fmt<kFmtE2M1H16, true>(a, s);
+    case kFmtE4M3:
+    case kFmtE4M3H16:
+    case kFmtE4M3H32: return launch_warp_row_fp8(a, s, true);
+    case kFmtE2M1:
+    case kFmtE2M1H16:
+    case kFmtE2M1H32: return launch_warp_row_fp4(a, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_mx_cast_warp_row(const WarpRowArgs& a, cudaStream_t s) {
-  switch (a.fmt) {
-    case kFmtE4M3: return launch_fmt<kFmtE4M3, false>(a, s);
-    case kFmtE2M1: return launch_fmt<kFmtE2M1, false>(a, s);
-    case kFmtE2M1H16: return launch_fmt<kFmtE2M1H16, false>(a, s);
-    default: return cudaErrorInvalidValue;
-  }
+  return launch_warp_row_fp8(a, s, false);
 }
 
 }  // namespace mxnorm

@@ -34,7 +34,12 @@ import numpy as np
 FMT_MXFP8_E4M3 = 0
 FMT_MXFP4_E2M1 = 1
 FMT_MXFP4_E2M1_H16 = 2
-FMT_NAMES = {"mxfp8": FMT_MXFP8_E4M3, "mxfp4": FMT_MXFP4_E2M1, "mxfp4_h16": FMT_MXFP4_E2M1_H16}
+FMT_MXFP8_E4M3_H16 = 3
+FMT_MXFP4_E2M1_H32 = 4
+FMT_MXFP8_E4M3_H32 = 5
+FMT_NAMES = {"mxfp8": FMT_MXFP8_E4M3, "mxfp4": FMT_MXFP4_E2M1, "mxfp4_h16": FMT_MXFP4_E2M1_H16,
+             "mxfp8_h16": FMT_MXFP8_E4M3_H16, "mxfp4_h32": FMT_MXFP4_E2M1_H32, "mxfp8_h32": FMT_MXFP8_E4M3_H32}
+FP8_FMTS = (FMT_MXFP8_E4M3, FMT_MXFP8_E4M3_H16, FMT_MXFP8_E4M3_H32)
 BLOCK = 32
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -71,6 +76,7 @@ def _load():
     lib.oracle_cast_e2m1_array.argtypes = [p, i64, p]
     lib.oracle_e8m0_exponent_array.argtypes = [p, i64, i32, p]
     lib.oracle_h16_groups.argtypes = [p, i64, p]
+    lib.oracle_h32_groups.argtypes = [p, i64, p]
     lib.oracle_float_to_bf16_array.argtypes = [p, i64, p]
     lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
     lib.oracle_decode_e4m3.restype = ctypes.c_double
@@ -96,7 +102,7 @@ def _as_bf16_bits(x) -> np.ndarray:
 
 
 def code_bytes_per_row(H: int, fmt) -> int:
-    return H if _fmt_id(fmt) == FMT_MXFP8_E4M3 else H // 2
+    return H if _fmt_id(fmt) in FP8_FMTS else H // 2
 
 
 def mxnorm_quant(x_bits: np.ndarray, p: int = 2, fmt="mxfp8"):
@@ -183,6 +189,17 @@ def h16(v) -> np.ndarray:
         raise ValueError("h16 needs a multiple of 16 values")
     out = np.empty_like(a)
     lib.oracle_h16_groups(_ptr(a), a.size // 16, _ptr(out))
+    return out
+
+
+def h32(v) -> np.ndarray:
+    """H32 / sqrt(32) applied to each consecutive group of 32 fp32 values."""
+    lib = _load()
+    a = np.ascontiguousarray(v, dtype=np.float32)
+    if a.size % 32:
+        raise ValueError("h32 needs a multiple of 32 values")
+    out = np.empty_like(a)
+    lib.oracle_h32_groups(_ptr(a), a.size // 32, _ptr(out))
     return out
 
 

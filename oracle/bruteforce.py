@@ -111,6 +111,29 @@ def h16_fp32(group):
     return [round_to_fp32(x / 4) for x in v]
 
 
+def h32_fp32(group):
+    """H32 v / sqrt(32): fp32 butterfly stages h = 1 .. 16, then each value
+    times RN_fp32(1/sqrt(32)) rounded to fp32.  group: 32 Fractions."""
+    v = list(group)
+    h = 1
+    while h < 32:
+        for i in range(32):
+            if i & h == 0:
+                a, b = v[i], v[i + h]
+                v[i], v[i + h] = round_to_fp32(a + b), round_to_fp32(a - b)
+        h *= 2
+    c32 = _round_inv_power_mean(Fraction(32), 2)      # RN_fp32(32^(-1/2)), decided exactly
+    return [round_to_fp32(x * c32) for x in v]
+
+
+def _is_fp8(fmt: str) -> bool:
+    return fmt.startswith("mxfp8")
+
+
+def _rotation(fmt: str) -> int:
+    return 16 if fmt.endswith("_h16") else 32 if fmt.endswith("_h32") else 0
+
+
 # ------------------------------------------------------------------- cast
 def nearest_code(r: Fraction, table: dict, sign_bit: int) -> int:
     """Code whose value is nearest to r among all finite codes of the format
@@ -129,11 +152,11 @@ def nearest_code(r: Fraction, table: dict, sign_bit: int) -> int:
 def mx_block(values, signs, fmt: str):
     """Scale exponent and codes of one 32-element block of exact values
     (with their sign bits, which decide the sign of zero codes)."""
-    emax = 8 if fmt == "mxfp8" else 2
+    emax = 8 if _is_fp8(fmt) else 2
     amax = max(abs(v) for v in values)
     e = -127 if amax == 0 else max(-127, min(127, floor_log2(amax) - emax))
     s = Fraction(2) ** e
-    table = _E4M3 if fmt == "mxfp8" else _E2M1
+    table = _E4M3 if _is_fp8(fmt) else _E2M1
     return e, [nearest_code(v / s, table, sb) for v, sb in zip(values, signs)]
 
 
@@ -141,16 +164,18 @@ def mxnorm_row(bits_row, p: int, fmt: str):
     """MXNorm of one finite bf16 row (list of ints): (code bytes, scale
     codes, inv_rms as an exact fp32 value).
 
-    For fmt "mxfp4_h16" a rotated value that is exactly zero raises
-    ValueError: the sign IEEE arithmetic gives such a zero is not modelled
-    here, so callers use inputs whose rotations have no exact zeros."""
+    For the rotated formats (*_h16, *_h32) a rotated value that is exactly
+    zero raises ValueError: the sign IEEE arithmetic gives such a zero is not
+    modelled here, so callers use inputs whose rotations have no exact zeros."""
     H = len(bits_row)
     assert H % BLOCK == 0
     K = H // BLOCK
     vals, signs = [], []
-    if fmt == "mxfp4_h16":
-        for g in range(0, H, 16):
-            rot = h16_fp32([bf16_value(b) for b in bits_row[g:g + 16]])
+    rot_n = _rotation(fmt)
+    if rot_n:
+        rotate = h16_fp32 if rot_n == 16 else h32_fp32
+        for g in range(0, H, rot_n):
+            rot = rotate([bf16_value(b) for b in bits_row[g:g + rot_n]])
             if any(v == 0 for v in rot):
                 raise ValueError("rotated value is exactly zero")
             vals.extend(rot)
@@ -164,7 +189,7 @@ def mxnorm_row(bits_row, p: int, fmt: str):
         e, c = mx_block(vals[sl], signs[sl], fmt)
         scales.append(e + 127)
         s_pow_sum += Fraction(2) ** (p * e)          # s_k^p
-        if fmt == "mxfp8":
+        if _is_fp8(fmt):
             codes.extend(c)
         else:
             codes.extend(c[j] | (c[j + 1] << 4) for j in range(0, BLOCK, 2))

@@ -38,6 +38,9 @@
  *   - H16: fp32 butterfly, stages h = 1, 2, 4, 8 in that order, each pair
  *     (v_i, v_{i+h}) -> (v_i + v_{i+h}, v_i - v_{i+h}) rounded to fp32, then
  *     every value times 0.25 in fp32; no bf16 re-rounding.
+ *   - H32: the same fp32 butterfly with stages h = 1, 2, 4, 8, 16, then every
+ *     value times c32 = RN_fp32(1/sqrt(32)) in fp32 (the orthonormal
+ *     H32/sqrt(32)); the page names H32 but not its normalisation.
  *   - E2M1 packing: element 2i in the low nibble of byte i.
  *   - RMSNorm baseline: inv = RN_fp32(1/sqrt(mean(x^2) + eps)),
  *     y = RN_bf16(RN_fp32(x * inv)), then the MXFP8 cast of y.
@@ -52,6 +55,9 @@
 #define OR_FMT_MXFP8_E4M3 0
 #define OR_FMT_MXFP4_E2M1 1
 #define OR_FMT_MXFP4_E2M1_H16 2
+#define OR_FMT_MXFP8_E4M3_H16 3
+#define OR_FMT_MXFP4_E2M1_H32 4
+#define OR_FMT_MXFP8_E4M3_H32 5
 
 #define OR_BLOCK 32            /* MX block size B, [ABS]: "32x decrease" */
 #define OR_SCALE_NAN 0xFF      /* E8M0 NaN code, [OCP] section 5.4 */
@@ -189,16 +195,14 @@ int oracle_e8m0_exponent(double amax, int emax_elem)
 
 /* ------------------------------------------------------------------ H16 */
 
-/* y = (1/4) * H16 * v for one group of 16 fp32 values, H16 the Sylvester
- * Hadamard matrix in natural order, H16[i][j] = (-1)^popcount(i & j).
- * Butterfly stages h = 1, 2, 4, 8; each add/sub rounded to fp32, then the
- * 1/4 scale in fp32.  [MXFP4] Metodologia, item 3. */
-void oracle_h16_group(const float *in, float *out)
+/* Unnormalised Sylvester-Hadamard butterfly on n = 16 or 32 fp32 values in
+ * place: stages h = 1, 2, 4, ... n/2, each pair (v_i, v_{i+h}) with
+ * (i & h) == 0 replaced by (v_i + v_{i+h}, v_i - v_{i+h}) rounded to fp32.
+ * The result is H_n v with H_n[i][j] = (-1)^popcount(i & j). */
+static void hadamard_butterfly(float *v, int n)
 {
-    float v[16];
-    for (int i = 0; i < 16; ++i) v[i] = in[i];
-    for (int h = 1; h < 16; h <<= 1) {
-        for (int i = 0; i < 16; ++i) {
+    for (int h = 1; h < n; h <<= 1) {
+        for (int i = 0; i < n; ++i) {
             if ((i & h) == 0) {
                 float a = v[i], b = v[i + h];
                 float s = a + b;
@@ -208,21 +212,59 @@ void oracle_h16_group(const float *in, float *out)
             }
         }
     }
+}
+
+/* y = (1/4) * H16 * v for one group of 16 fp32 values, H16 the Sylvester
+ * Hadamard matrix in natural order, H16[i][j] = (-1)^popcount(i & j).
+ * Butterfly stages h = 1, 2, 4, 8; each add/sub rounded to fp32, then the
+ * 1/4 scale in fp32.  [MXFP4] Metodologia, item 3. */
+void oracle_h16_group(const float *in, float *out)
+{
+    float v[16];
+    for (int i = 0; i < 16; ++i) v[i] = in[i];
+    hadamard_butterfly(v, 16);
     for (int i = 0; i < 16; ++i) {
         float q = v[i] * 0.25f;
         out[i] = q;
     }
 }
 
+/* y = H32 * v / sqrt(32) for one group of 32 fp32 values: butterfly stages
+ * h = 1 .. 16 in fp32, then each value times RN_fp32(1/sqrt(32)) in fp32.
+ * [MXFP4] Metodologia, item 3 (H32). */
+void oracle_h32_group(const float *in, float *out)
+{
+    const float c32 = (float)(1.0 / sqrt(32.0));
+    float v[32];
+    for (int i = 0; i < 32; ++i) v[i] = in[i];
+    hadamard_butterfly(v, 32);
+    for (int i = 0; i < 32; ++i) {
+        float q = v[i] * c32;
+        out[i] = q;
+    }
+}
+
 /* -------------------------------------------------------------- helpers */
 
-static int emax_of(int fmt) { return fmt == OR_FMT_MXFP8_E4M3 ? 8 : 2; }
+static int is_fp8(int fmt)
+{
+    return fmt == OR_FMT_MXFP8_E4M3 || fmt == OR_FMT_MXFP8_E4M3_H16 || fmt == OR_FMT_MXFP8_E4M3_H32;
+}
+
+/* rotation size applied before the cast: 0 (none), 16 or 32 */
+static int rotation_of(int fmt)
+{
+    if (fmt == OR_FMT_MXFP4_E2M1_H16 || fmt == OR_FMT_MXFP8_E4M3_H16) return 16;
+    if (fmt == OR_FMT_MXFP4_E2M1_H32 || fmt == OR_FMT_MXFP8_E4M3_H32) return 32;
+    return 0;
+}
+
+static int emax_of(int fmt) { return is_fp8(fmt) ? 8 : 2; }
 
 static int check_args(int64_t T, int64_t H, int fmt)
 {
     if (T < 0 || H <= 0 || H % OR_BLOCK != 0) return 1;
-    if (fmt != OR_FMT_MXFP8_E4M3 && fmt != OR_FMT_MXFP4_E2M1 &&
-        fmt != OR_FMT_MXFP4_E2M1_H16) return 1;
+    if (fmt < OR_FMT_MXFP8_E4M3 || fmt > OR_FMT_MXFP8_E4M3_H32) return 1;
     return 0;
 }
 
@@ -231,13 +273,19 @@ static int check_args(int64_t T, int64_t H, int fmt)
 static void block_values(const uint16_t *row, int64_t k, int fmt, double *v)
 {
     const uint16_t *b = row + k * OR_BLOCK;
-    if (fmt == OR_FMT_MXFP4_E2M1_H16) {
+    const int rot = rotation_of(fmt);
+    if (rot == 16) {
         for (int g = 0; g < OR_BLOCK; g += 16) {
             float in[16], out[16];
             for (int i = 0; i < 16; ++i) in[i] = bf16_bits_to_float(b[g + i]);
             oracle_h16_group(in, out);
             for (int i = 0; i < 16; ++i) v[g + i] = (double)out[i];
         }
+    } else if (rot == 32) {
+        float in[32], out[32];
+        for (int i = 0; i < 32; ++i) in[i] = bf16_bits_to_float(b[i]);
+        oracle_h32_group(in, out);
+        for (int i = 0; i < 32; ++i) v[i] = (double)out[i];
     } else {
         for (int j = 0; j < OR_BLOCK; ++j) v[j] = (double)bf16_bits_to_float(b[j]);
     }
@@ -256,7 +304,7 @@ static int cast_block(const double *v, int fmt, uint8_t *scale_out,
     }
     if (!finite) {
         *scale_out = OR_SCALE_NAN;
-        if (fmt == OR_FMT_MXFP8_E4M3)
+        if (is_fp8(fmt))
             for (int j = 0; j < OR_BLOCK; ++j) codes_row[k * OR_BLOCK + j] = 0x7F;
         else
             for (int j = 0; j < OR_BLOCK / 2; ++j) codes_row[k * (OR_BLOCK / 2) + j] = 0x00;
@@ -264,7 +312,7 @@ static int cast_block(const double *v, int fmt, uint8_t *scale_out,
     }
     int e = oracle_e8m0_exponent(amax, emax_of(fmt));
     *scale_out = (uint8_t)(e + 127);
-    if (fmt == OR_FMT_MXFP8_E4M3) {
+    if (is_fp8(fmt)) {
         for (int j = 0; j < OR_BLOCK; ++j)
             codes_row[k * OR_BLOCK + j] = oracle_cast_e4m3(ldexp(v[j], -e));
     } else {
@@ -286,7 +334,7 @@ int oracle_mx_cast_rows(const uint16_t *x, int64_t T, int64_t H, int fmt,
 {
     if (check_args(T, H, fmt)) return 1;
     const int64_t K = H / OR_BLOCK;
-    const int64_t code_bytes = (fmt == OR_FMT_MXFP8_E4M3) ? H : H / 2;
+    const int64_t code_bytes = is_fp8(fmt) ? H : H / 2;
     double v[OR_BLOCK];
     for (int64_t t = 0; t < T; ++t) {
         const uint16_t *row = x + t * H;
@@ -312,7 +360,7 @@ int oracle_mxnorm_rows(const uint16_t *x, int64_t T, int64_t H, int p, int fmt,
     if (check_args(T, H, fmt)) return 1;
     if (p != 1 && p != 2) return 1;
     const int64_t K = H / OR_BLOCK;
-    const int64_t code_bytes = (fmt == OR_FMT_MXFP8_E4M3) ? H : H / 2;
+    const int64_t code_bytes = is_fp8(fmt) ? H : H / 2;
     double v[OR_BLOCK];
     for (int64_t t = 0; t < T; ++t) {
         const uint16_t *row = x + t * H;
@@ -382,6 +430,11 @@ void oracle_e8m0_exponent_array(const double *amax, int64_t n, int emax_elem, in
 void oracle_h16_groups(const float *in, int64_t n_groups, float *out)
 {
     for (int64_t g = 0; g < n_groups; ++g) oracle_h16_group(in + 16 * g, out + 16 * g);
+}
+
+void oracle_h32_groups(const float *in, int64_t n_groups, float *out)
+{
+    for (int64_t g = 0; g < n_groups; ++g) oracle_h32_group(in + 32 * g, out + 32 * g);
 }
 
 void oracle_float_to_bf16_array(const float *in, int64_t n, uint16_t *out)

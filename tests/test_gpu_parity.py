@@ -19,7 +19,7 @@ from mx_scale_reusing_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 INV_RTOL = 1e-6
-FMTS = ["mxfp8", "mxfp4", "mxfp4_h16"]
+FMTS = ["mxfp8", "mxfp4", "mxfp4_h16", "mxfp8_h16", "mxfp4_h32", "mxfp8_h32"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -156,6 +156,8 @@ def sample_rows(T, n=192, seed=0):
     ("llama3_1b_32768x2048", "mxfp8", (2,)),
     ("llama3_8b_65536x4096", "mxfp8", (1, 2)),
     ("llama3_8b_mxfp4_h16_65536x4096", "mxfp4_h16", (2,)),
+    ("llama3_8b_mxfp4_h16_65536x4096", "mxfp4_h32", (2,)),
+    ("llama3_8b_mxfp4_h16_65536x4096", "mxfp8_h16", (2,)),
 ])
 def test_full_size_workloads_sampled_rows(name, fmt, ps):
     """Full-size inputs in the launch configuration the benchmark times
@@ -171,7 +173,7 @@ def test_full_size_workloads_sampled_rows(name, fmt, ps):
             c2, s2, i2 = run(xb, p, fmt, v)
             assert np.array_equal(c2, c) and np.array_equal(s2, s) and np.array_equal(i2, i), v
         assert s.min() >= 0 and s.max() <= 254
-        if fmt == "mxfp8":
+        if fmt.startswith("mxfp8"):
             assert not ((c & 0x7F) == 0x7F).any()
         e = s.astype(np.float64) - 127
         mean = np.exp2(p * e).mean(1)

@@ -158,6 +158,57 @@ def test_h16_closed_forms(oracle_mod):
     np.testing.assert_array_equal(oracle_mod.h16(oracle_mod.h16(v)), v)
 
 
+def test_h32_butterfly_matches_sylvester_matrix(oracle_mod):
+    """On small integers the fp32 butterfly is exact, so the oracle's H32 /
+    sqrt(32) equals the exact product with scipy's Sylvester hadamard(32)
+    followed by one fp32 multiply with RN_fp32(1/sqrt(32))."""
+    from scipy.linalg import hadamard
+    Hm = hadamard(32).astype(np.float64)
+    rng = np.random.default_rng(7)
+    v = rng.integers(-500, 500, size=(64, 32)).astype(np.float32)
+    exact = (v.astype(np.float64) @ Hm.T)                   # integers, exact in fp32
+    c32 = np.float32(1.0 / np.sqrt(32.0))
+    assert c32 == np.float32(0.17677669)
+    want = (exact.astype(np.float32) * c32).astype(np.float32)
+    np.testing.assert_array_equal(oracle_mod.h32(v).reshape(64, 32), want)
+
+
+def test_h32_closed_forms(oracle_mod):
+    e0 = np.zeros(32, np.float32)
+    e0[0] = 1
+    np.testing.assert_array_equal(oracle_mod.h32(e0), np.full(32, np.float32(1 / np.sqrt(32)), np.float32))
+    c = np.full(32, 2.0, np.float32)
+    out = oracle_mod.h32(c)
+    assert out[0] == np.float32(np.float32(64.0) * np.float32(1 / np.sqrt(32))) and (out[1:] == 0).all()
+    rng = np.random.default_rng(8)
+    v = rng.standard_normal((500, 32)).astype(np.float32)
+    y = oracle_mod.h32(v).reshape(500, 32).astype(np.float64)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(v.astype(np.float64), axis=1), rtol=2e-6)
+    # (H32/sqrt 32)^2 = I up to the fp32 roundings of the two passes
+    np.testing.assert_allclose(oracle_mod.h32(oracle_mod.h32(v)).reshape(500, 32), v, rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("fmt,rot", [("mxfp8_h16", 16), ("mxfp4_h32", 32), ("mxfp8_h32", 32)])
+def test_rotated_formats_cast_the_rotated_values(oracle_mod, fmt, rot):
+    """A rotated format equals the plain MX cast applied to the rotation's
+    output (the rotation runs first, per aligned group), checked through the
+    independent per-element casts."""
+    x = synth.make_random_rows(4, 256, seed=9, scale=2.0)
+    codes, scales, inv = oracle_mod.mxnorm_quant(x, 2, fmt)
+    v = synth.bf16_bits_to_f32(x)
+    y = (oracle_mod.h16 if rot == 16 else oracle_mod.h32)(v).reshape(v.shape).astype(np.float64)
+    amax = np.abs(y).reshape(4, 8, 32).max(-1)
+    emax = 8 if fmt.startswith("mxfp8") else 2
+    e = oracle_mod.e8m0_exponent(amax, emax)
+    np.testing.assert_array_equal(scales, e + 127)
+    r = y / np.repeat(np.exp2(e.astype(np.float64)), 32, axis=1)
+    if fmt.startswith("mxfp8"):
+        np.testing.assert_array_equal(codes, oracle_mod.cast_e4m3(r))
+    else:
+        nib = oracle_mod.cast_e2m1(r)
+        np.testing.assert_array_equal(codes, nib[:, 0::2] | (nib[:, 1::2] << 4))
+
+
 def test_h16_preserves_norm(oracle_mod):
     rng = np.random.default_rng(4)
     v = rng.standard_normal((1000, 16)).astype(np.float32)
@@ -246,7 +297,8 @@ def test_nonfinite_block_reading(oracle_mod):
 
 
 # ----------------------------------------------------------- invariants
-@pytest.mark.parametrize("fmt,emax,qmax", [("mxfp8", 8, 448.0), ("mxfp4", 2, 6.0), ("mxfp4_h16", 2, 6.0)])
+@pytest.mark.parametrize("fmt,emax,qmax", [("mxfp8", 8, 448.0), ("mxfp4", 2, 6.0), ("mxfp4_h16", 2, 6.0),
+                                           ("mxfp8_h16", 8, 448.0), ("mxfp4_h32", 2, 6.0), ("mxfp8_h32", 8, 448.0)])
 @pytest.mark.parametrize("p", [1, 2])
 def test_cast_and_growth_invariants(oracle_mod, fmt, emax, qmax, p):
     """|dec(q)| <= qmax; |dec(q) - x/s| <= half a grid step unless saturated;
@@ -258,11 +310,13 @@ def test_cast_and_growth_invariants(oracle_mod, fmt, emax, qmax, p):
     codes, scales, inv = oracle_mod.mxnorm_quant(x, p, fmt)
     K = w.K
     v = synth.bf16_bits_to_f32(x).astype(np.float64)
-    if fmt == "mxfp4_h16":
+    if fmt.endswith("_h16"):
         v = oracle_mod.h16(v.astype(np.float32)).reshape(v.shape).astype(np.float64)
+    elif fmt.endswith("_h32"):
+        v = oracle_mod.h32(v.astype(np.float32)).reshape(v.shape).astype(np.float64)
     s = np.exp2(scales.astype(np.float64) - 127)
     r = v / np.repeat(s, 32, axis=1)
-    if fmt == "mxfp8":
+    if fmt.startswith("mxfp8"):
         dec = np.vectorize(oracle_mod.decode_e4m3)(codes)
         grid = np.array([oracle_mod.decode_e4m3(c) for c in range(127)])
     else:
@@ -315,7 +369,7 @@ def test_tiny_workload_vs_bruteforce(oracle_mod):
     _check_rows_vs_bruteforce(oracle_mod, synth.make_activations(w), 2, "mxfp8")
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "mxfp4_h16"])
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "mxfp4_h16", "mxfp8_h16", "mxfp4_h32", "mxfp8_h32"])
 @pytest.mark.parametrize("p", [1, 2])
 @pytest.mark.parametrize("H", [32, 64, 96, 256])
 def test_random_tiny_rows_vs_bruteforce(oracle_mod, fmt, p, H):
