@@ -44,6 +44,12 @@
  *   - E2M1 packing: element 2i in the low nibble of byte i.
  *   - RMSNorm baseline: inv = RN_fp32(1/sqrt(mean(x^2) + eps)),
  *     y = RN_bf16(RN_fp32(x * inv)), then the MXFP8 cast of y.
+ *   - Backward (straight-through estimator, [MXN] section 2, "Gradientes":
+ *     RMSNorm's gradient logic reused, nothing saved but the normaliser):
+ *     the cast is treated as the identity and RMSNorm's backward runs with
+ *     the saved estimate rho~ in place of 1/RMS,
+ *       dx = rho~ * dy - rho~^3 * x * (1/H) * sum_j dy_j x_j,
+ *     evaluated in fp64 and rounded once to bf16.
  *
  * Arithmetic: fp64 throughout (every intermediate value of the cast is exact
  * in fp64; the power-mean sum carries a relative error below K * 2^-53).
@@ -91,6 +97,28 @@ static uint16_t float_to_bf16_rne(float f)
     if (dist_lo < dist_hi) return lo;
     if (dist_hi < dist_lo) return hi;
     return (lo & 1u) ? hi : lo;
+}
+
+/* Round a double to the nearest bf16 (ties to an even last bit); finite
+ * values within the bf16 range only.  The two bf16 neighbours are found
+ * from the float nearest below in magnitude and compared exactly. */
+static uint16_t double_to_bf16_rne(double d)
+{
+    if (isnan(d)) return 0x7FC0;
+    double a = fabs(d);
+    /* largest bf16 magnitude <= a: truncate the float of a toward zero */
+    float f = (float)a;
+    if ((double)f > a) f = nextafterf(f, 0.0f);
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t lo = (uint16_t)(u >> 16);
+    if ((double)bf16_bits_to_float(lo) > a) lo = (uint16_t)(lo - 1);
+    uint16_t hi = (uint16_t)(lo + 1);
+    double dlo = a - (double)bf16_bits_to_float(lo);
+    double dhi = (double)bf16_bits_to_float(hi) - a;
+    uint16_t m = (dlo < dhi) ? lo : (dhi < dlo) ? hi : ((lo & 1u) ? hi : lo);
+    if (dlo == 0.0) m = lo;
+    return (uint16_t)(m | (signbit(d) ? 0x8000u : 0u));
 }
 
 /* ------------------------------------------------------- element grids */
@@ -408,6 +436,29 @@ int oracle_rmsnorm_mxfp8_rows(const uint16_t *x, int64_t T, int64_t H, float eps
         }
     }
     return oracle_mx_cast_rows(y, T, H, OR_FMT_MXFP8_E4M3, codes, scales);
+}
+
+/* ------------------------------------------------------------ backward */
+
+/* Straight-through backward of T rows: x, dy bf16 [T, H], inv_rms [T] (the
+ * forward's rho~), dx bf16 [T, H].  fp64 throughout, one bf16 rounding. */
+int oracle_mxnorm_bwd_ste_rows(const uint16_t *x, const uint16_t *dy, const float *inv_rms,
+                               int64_t T, int64_t H, uint16_t *dx)
+{
+    if (T < 0 || H <= 0) return 1;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t *xr = x + t * H, *gr = dy + t * H;
+        double dot = 0.0;
+        for (int64_t j = 0; j < H; ++j)
+            dot += (double)bf16_bits_to_float(gr[j]) * (double)bf16_bits_to_float(xr[j]);
+        const double r = (double)inv_rms[t];
+        const double k = r * r * r * dot / (double)H;
+        for (int64_t j = 0; j < H; ++j) {
+            const double g = r * (double)bf16_bits_to_float(gr[j]) - k * (double)bf16_bits_to_float(xr[j]);
+            dx[t * H + j] = double_to_bf16_rne(g);
+        }
+    }
+    return 0;
 }
 
 /* ------------------------------------------------- array entry points */

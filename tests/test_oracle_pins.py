@@ -424,3 +424,62 @@ def test_h16_rotation_preserves_row_rms(oracle_mod):
     v = synth.bf16_bits_to_f32(x).astype(np.float32)
     y = oracle_mod.h16(v).reshape(v.shape).astype(np.float64)
     np.testing.assert_allclose(np.sqrt((y ** 2).mean(1)), np.sqrt((v.astype(np.float64) ** 2).mean(1)), rtol=1e-6)
+
+
+# ------------------------------------------------------- backward (STE)
+def _rms_inv(xv):
+    return 1.0 / np.sqrt((xv.astype(np.float64) ** 2).mean(-1))
+
+
+def test_bwd_matches_finite_differences_of_rmsnorm(oracle_mod):
+    """With the exact 1/RMS as the saved normaliser, the straight-through
+    backward is RMSNorm's exact gradient: compare with central differences of
+    L(x) = sum_j w_j x_j / RMS(x) in fp64 ("MXNorm ...", Gradientes)."""
+    rng = np.random.default_rng(12)
+    T, H = 3, 64
+    xb = synth.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    wb = synth.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    xv = synth.bf16_bits_to_f32(xb).astype(np.float64)
+    wv = synth.bf16_bits_to_f32(wb).astype(np.float64)
+    inv = _rms_inv(xv).astype(np.float32)
+    dx = synth.bf16_bits_to_f32(oracle_mod.mxnorm_bwd_ste(xb, wb, inv)).astype(np.float64)
+
+    def L(row, t):
+        return float((wv[t] * row).sum() / np.sqrt((row ** 2).mean()))
+
+    for t in range(T):
+        fd = np.empty(H)
+        for i in range(H):
+            h = 1e-6 * max(1.0, abs(xv[t, i]))
+            e = np.zeros(H)
+            e[i] = h
+            fd[i] = (L(xv[t] + e, t) - L(xv[t] - e, t)) / (2 * h)
+        scale = np.abs(fd).max()
+        assert np.abs(dx[t] - fd).max() <= 2.0 ** -7 * scale, t
+
+
+def test_bwd_is_orthogonal_to_x_for_the_exact_normaliser(oracle_mod):
+    """RMSNorm is scale invariant, so its gradient is orthogonal to x:
+    sum_j dx_j x_j = 0 (up to the bf16 rounding of dx)."""
+    x = synth.make_activations(synth.WORKLOADS["llama3_1b_32768x2048"], rows=4)
+    dyb = synth.make_random_rows(4, 2048, seed=13)
+    xv = synth.bf16_bits_to_f32(x).astype(np.float64)
+    dx = synth.bf16_bits_to_f32(oracle_mod.mxnorm_bwd_ste(x, dyb, _rms_inv(xv).astype(np.float32))).astype(np.float64)
+    dot = (dx * xv).sum(1)
+    assert (np.abs(dot) <= 2.0 ** -7 * (np.abs(dx) * np.abs(xv)).sum(1)).all()
+
+
+def test_bwd_closed_forms(oracle_mod):
+    """dy orthogonal to x: dx = rho dy exactly (then bf16); dy = y = rho x with
+    rho = 1/RMS: dx = 0."""
+    H = 32
+    x = np.zeros((2, H), np.float32)
+    x[:, 0] = 2.0
+    dy = np.zeros((2, H), np.float32)
+    dy[0, 1:] = np.linspace(-1, 1, H - 1)
+    inv = np.array([0.75, 1.0 / np.sqrt(4.0 / H)], np.float32)
+    dy[1] = x[1] * inv[1]
+    dx = synth.bf16_bits_to_f32(oracle_mod.mxnorm_bwd_ste(synth.f32_to_bf16_bits(x), synth.f32_to_bf16_bits(dy), inv))
+    want0 = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits((0.75 * synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(dy[0]))).astype(np.float32)))
+    np.testing.assert_array_equal(dx[0], want0)
+    assert np.abs(dx[1]).max() <= 1e-6
