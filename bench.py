@@ -244,6 +244,23 @@ def run_gpu(args):
     m = statistics.fmean(perw)
     extra["mxnorm_mxfp8_p2_warp_row"] = {"ms": round(m, 5), "GB/s": gbs(abytes, m), "frac": round(gbs(abytes, m) / hbm_peak, 4)}
 
+    # straight-through backward on the same rows (dy ~ N(0,1), inv from the forward)
+    dy = torch.randn((T, H), device=dev, generator=torch.Generator(device=dev).manual_seed(5)).to(torch.bfloat16)
+    dxs = [torch.empty_like(dy) for _ in range(nbuf)]
+
+    def bwd_step(i):
+        st = mx.lib().mxnorm_bwd_ste(xs[i].data_ptr(), dy.data_ptr(), outs[i][2].data_ptr(), T, H,
+                                     dxs[i].data_ptr(), ctypes.c_void_p(sptr))
+        if st:
+            raise RuntimeError(mx.lib().mxnorm_last_error().decode())
+
+    perbw, _ = time_launches(torch, stream, bwd_step, sec_steps, 5, nbuf)
+    m = statistics.fmean(perbw)
+    extra["mxnorm_bwd_ste"] = {"ms": round(m, 5), "GB/s": gbs(T * (6 * H + 4), m),
+                               "frac": round(gbs(T * (6 * H + 4), m) / hbm_peak, 4),
+                               "bytes_per_row": 6 * H + 4}
+    del dy, dxs
+
     y_ws = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
 
     def base_step(i):

@@ -124,6 +124,22 @@ int mxnorm_quant_fwd_ex(const void* x, int64_t T, int64_t H, int p, int fmt, voi
 int rmsnorm_mxfp8_ref_fwd(const void* x, int64_t T, int64_t H, float eps, void* y_workspace,
                           uint8_t* codes, uint8_t* scales, float* inv_rms, void* stream);
 
+/* Straight-through backward of MXNorm ("MXNorm ...", Resumen tecnico,
+ * 2. Metodologia, "Gradientes": RMSNorm's gradient logic reused through a
+ * straight-through estimator, nothing kept but what RMSNorm keeps).  The MX
+ * cast counts as the identity and RMSNorm's backward runs with the forward's
+ * estimate rho~ = inv_rms in place of 1/RMS:
+ *     dx = rho~ * dy - rho~^3 * x * (1/H) * sum_j dy_j * x_j
+ * (fp32 arithmetic, dx rounded to bf16).  Works as plain RMSNorm's backward
+ * when inv_rms holds the exact 1/RMS.
+ *   x        bf16 [T, H]  the forward's input            16-byte aligned
+ *   dy       bf16 [T, H]  gradient w.r.t. x * rho~        16-byte aligned
+ *   inv_rms  f32  [T]     the forward's estimate           4-byte aligned
+ *   dx       bf16 [T, H]  output                           16-byte aligned
+ * Errors and stream semantics as mxnorm_quant_fwd. */
+int mxnorm_bwd_ste(const void* x, const void* dy, const float* inv_rms, int64_t T, int64_t H, void* dx,
+                   void* stream);
+
 /* Allocation-free form of rmsnorm_mxfp8_ref_fwd.  The paper has no
  * counterpart: this exists for callers that cannot allocate device memory
  * (a host framework that owns every allocation through its own pool, a

@@ -19,7 +19,7 @@ import os
 __all__ = [
     "FMT", "VARIANT", "MXNormError", "MXNormLibraryMissing", "lib", "library_path",
     "mxnorm_quant_fwd", "quant_fwd", "quant_fwd_host", "rmsnorm_mxfp8_ref_fwd", "device_errors",
-    "code_bytes",
+    "code_bytes", "bwd_ste",
 ]
 
 FMT = {"mxfp8": 0, "mxfp4": 1, "mxfp4_h16": 2, "mxfp8_h16": 3, "mxfp4_h32": 4, "mxfp8_h32": 5}
@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
     L.mxnorm_last_error.argtypes = []
     L.mxnorm_last_error.restype = ctypes.c_char_p
     L.mxnorm_abi_version.restype = i32
+    L.mxnorm_bwd_ste.argtypes = [vp, vp, vp, i64, i64, vp, vp]
+    L.mxnorm_bwd_ste.restype = i32
     L.mxnorm_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     L.mxnorm_device_errors.restype = i32
     _lib = L
@@ -135,6 +137,26 @@ def rmsnorm_mxfp8_ref_fwd(x, eps: float = 1e-5, out=None, stream=None):
     _check(lib().rmsnorm_mxfp8_ref_fwd(x.data_ptr(), T, H, float(eps), y.data_ptr(), codes.data_ptr(),
                                        scales.data_ptr(), inv.data_ptr(), _stream_ptr(x.device, stream)))
     return y, codes, scales, inv
+
+
+def bwd_ste(x, dy, inv_rms, out=None, stream=None):
+    """Straight-through backward of MXNorm: dx = r dy - r^3 x mean(dy x)
+    with r = inv_rms from the forward.  x, dy: contiguous bf16 CUDA tensors
+    [..., H]; inv_rms: float32 [...].  Returns dx (bf16, like x)."""
+    import torch
+    for t in (x, dy):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+            raise ValueError("x and dy must be contiguous bfloat16 CUDA tensors")
+    if dy.shape != x.shape or inv_rms.dtype != torch.float32 or not inv_rms.is_contiguous():
+        raise ValueError("dy must match x, inv_rms must be contiguous float32")
+    H = x.shape[-1]
+    T = x.numel() // H if H else 0
+    if inv_rms.numel() != T:
+        raise ValueError("inv_rms needs one value per row")
+    dx = torch.empty_like(x) if out is None else out
+    _check(lib().mxnorm_bwd_ste(x.data_ptr(), dy.data_ptr(), inv_rms.data_ptr(), T, H, dx.data_ptr(),
+                                _stream_ptr(x.device, stream)))
+    return dx
 
 
 def device_errors(clear: bool = True) -> int:

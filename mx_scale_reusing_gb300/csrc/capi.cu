@@ -126,6 +126,24 @@ int rmsnorm_mxfp8_ref_fwd(const void* x, int64_t T, int64_t H, float eps, void* 
   return MXNORM_OK;
 }
 
+int mxnorm_bwd_ste(const void* x, const void* dy, const float* inv_rms, int64_t T, int64_t H, void* dx,
+                   void* stream) {
+  g_last_error.clear();
+  if (T < 0) return fail(MXNORM_ERR_INVALID_ARG, "T = %lld < 0", (long long)T);
+  if (H <= 0 || H % kBlock != 0)
+    return fail(MXNORM_ERR_INVALID_ARG, "H = %lld is not a positive multiple of 32", (long long)H);
+  if (H > MXNORM_MAX_H)
+    return fail(MXNORM_ERR_UNSUPPORTED, "H = %lld exceeds MXNORM_MAX_H = %d", (long long)H, MXNORM_MAX_H);
+  if (T == 0) return MXNORM_OK;
+  if (!x || !dy || !inv_rms || !dx) return fail(MXNORM_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(x, 16) || !aligned(dy, 16) || !aligned(dx, 16))
+    return fail(MXNORM_ERR_MISALIGNED, "x, dy and dx must be 16-byte aligned");
+  if (!aligned(inv_rms, 4)) return fail(MXNORM_ERR_MISALIGNED, "inv_rms is not 4-byte aligned");
+  cudaError_t err = launch_mxnorm_bwd_ste(BwdArgs{x, dy, inv_rms, T, H, dx}, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "mxnorm_bwd_ste launch");
+  return MXNORM_OK;
+}
+
 const char* mxnorm_status_string(int status) {
   switch (status) {
     case MXNORM_OK: return "MXNORM_OK";

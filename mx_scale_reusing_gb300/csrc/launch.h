@@ -27,6 +27,15 @@ struct RmsNormArgs {
   float* inv_rms;     // f32 [T]
 };
 
+struct BwdArgs {
+  const void* x;       // bf16 [T, H], the forward's input
+  const void* dy;      // bf16 [T, H], gradient w.r.t. the normalised output
+  const float* inv_rms;  // f32 [T], the forward's estimate
+  int64_t T;
+  int64_t H;
+  void* dx;            // bf16 [T, H]
+};
+
 struct TiledArgs {
   WarpRowArgs base;
   unsigned int* error_flag;  // device word set when a bounded wait gives up
@@ -42,6 +51,7 @@ cudaError_t launch_mx_cast_warp_row(const WarpRowArgs& a, cudaStream_t s);
 cudaError_t launch_rmsnorm_bf16(const RmsNormArgs& a, cudaStream_t s);
 cudaError_t launch_mxnorm_tiled(const TiledArgs& a, cudaStream_t s);
 bool tiled_supported(int64_t H, int fmt);
+cudaError_t launch_mxnorm_bwd_ste(const BwdArgs& a, cudaStream_t s);
 
 // Replace the calling thread's message returned by mxnorm_last_error().
 void set_last_error(const char* msg);

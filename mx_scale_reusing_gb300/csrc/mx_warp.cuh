@@ -75,7 +75,7 @@ template <int FMT, int VEC, int NCHUNK>
 struct StreamTuning {
   static constexpr bool fp4 = FmtTraits<FMT>::fp4;
   static constexpr int ahead = (VEC == 8) ? NCHUNK
-                               : (VEC == 32) ? (FmtTraits<FMT>::fp4 ? 1 : 2)
+                               : (VEC == 32) ? ((!FmtTraits<FMT>::fp4 && NCHUNK % 2 == 0) ? 2 : 1)
                                : (fp4 && NCHUNK % 2 == 0) ? 2 : (NCHUNK == 2 ? 2 : 1);
   static constexpr int minb = (VEC == 32) ? 2
                               : (VEC == 8 && NCHUNK == 1) ? 8 : (!fp4 && NCHUNK >= 8) ? 3 : 4;

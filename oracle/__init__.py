@@ -78,7 +78,7 @@ def _load():
     lib.oracle_h16_groups.argtypes = [p, i64, p]
     lib.oracle_h32_groups.argtypes = [p, i64, p]
     lib.oracle_float_to_bf16_array.argtypes = [p, i64, p]
-    lib.oracle_mxnorm_bwd_ste_rows.argtypes = [p, p, p, i64, i64, p]
+    lib.oracle_mxnorm_bwd_ste_rows.argtypes = [p, p, p, i64, i64, p, p]
     lib.oracle_mxnorm_bwd_ste_rows.restype = i32
     lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
     lib.oracle_decode_e4m3.restype = ctypes.c_double
@@ -156,10 +156,11 @@ def rmsnorm_mxfp8(x_bits: np.ndarray, eps: float = 1e-5):
     return y, codes, scales, inv
 
 
-def mxnorm_bwd_ste(x_bits: np.ndarray, dy_bits: np.ndarray, inv_rms: np.ndarray) -> np.ndarray:
+def mxnorm_bwd_ste(x_bits: np.ndarray, dy_bits: np.ndarray, inv_rms: np.ndarray, with_f64: bool = False):
     """Straight-through backward: dx = r dy - r^3 x mean(dy x) with r the
     forward's inv_rms ("MXNorm ...", 2. Metodologia, Gradientes: RMSNorm's
-    gradient logic reused).  Returns dx as bf16 bits [T, H]."""
+    gradient logic reused).  Returns dx as bf16 bits [T, H] (and the
+    unrounded fp64 values when with_f64)."""
     lib = _load()
     x = _as_bf16_bits(x_bits)
     dy = _as_bf16_bits(dy_bits)
@@ -168,9 +169,11 @@ def mxnorm_bwd_ste(x_bits: np.ndarray, dy_bits: np.ndarray, inv_rms: np.ndarray)
     if dy.shape != x.shape or inv.shape != (T,):
         raise ValueError("shape mismatch")
     dx = np.empty((T, H), np.uint16)
-    if lib.oracle_mxnorm_bwd_ste_rows(_ptr(x), _ptr(dy), _ptr(inv), T, H, _ptr(dx)) != 0:
+    dx64 = np.empty((T, H), np.float64) if with_f64 else None
+    if lib.oracle_mxnorm_bwd_ste_rows(_ptr(x), _ptr(dy), _ptr(inv), T, H, _ptr(dx),
+                                      _ptr(dx64) if with_f64 else None) != 0:
         raise ValueError("oracle rejected arguments")
-    return dx
+    return (dx, dx64) if with_f64 else dx
 
 
 def cast_e4m3(r) -> np.ndarray:

@@ -441,9 +441,10 @@ int oracle_rmsnorm_mxfp8_rows(const uint16_t *x, int64_t T, int64_t H, float eps
 /* ------------------------------------------------------------ backward */
 
 /* Straight-through backward of T rows: x, dy bf16 [T, H], inv_rms [T] (the
- * forward's rho~), dx bf16 [T, H].  fp64 throughout, one bf16 rounding. */
+ * forward's rho~), dx bf16 [T, H] (and, if dx64 is not NULL, the unrounded
+ * fp64 values).  fp64 throughout, one bf16 rounding. */
 int oracle_mxnorm_bwd_ste_rows(const uint16_t *x, const uint16_t *dy, const float *inv_rms,
-                               int64_t T, int64_t H, uint16_t *dx)
+                               int64_t T, int64_t H, uint16_t *dx, double *dx64)
 {
     if (T < 0 || H <= 0) return 1;
     for (int64_t t = 0; t < T; ++t) {
@@ -456,6 +457,7 @@ int oracle_mxnorm_bwd_ste_rows(const uint16_t *x, const uint16_t *dy, const floa
         for (int64_t j = 0; j < H; ++j) {
             const double g = r * (double)bf16_bits_to_float(gr[j]) - k * (double)bf16_bits_to_float(xr[j]);
             dx[t * H + j] = double_to_bf16_rne(g);
+            if (dx64) dx64[t * H + j] = g;
         }
     }
     return 0;

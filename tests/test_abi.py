@@ -76,6 +76,16 @@ def test_null_and_misaligned_pointers(L):
     assert L.rmsnorm_mxfp8_ref_fwd(FAKE, 0, 64, 1e-5, FAKE, FAKE, FAKE, FAKE, None) == 0
 
 
+def test_bwd_validation(L):
+    assert L.mxnorm_bwd_ste(FAKE, FAKE, FAKE, 0, 4096, FAKE, None) == 0
+    assert L.mxnorm_bwd_ste(FAKE, FAKE, FAKE, -1, 4096, FAKE, None) == 1
+    assert L.mxnorm_bwd_ste(FAKE, FAKE, FAKE, 8, 100, FAKE, None) == 1
+    assert L.mxnorm_bwd_ste(FAKE, None, FAKE, 8, 128, FAKE, None) == 1
+    assert L.mxnorm_bwd_ste(FAKE, FAKE + 8, FAKE, 8, 128, FAKE, None) == 3
+    assert L.mxnorm_bwd_ste(FAKE, FAKE, FAKE + 1, 8, 128, FAKE, None) == 3
+    assert L.mxnorm_bwd_ste(FAKE, FAKE, FAKE, 8, (1 << 20) + 32, FAKE, None) == 2
+
+
 def test_python_binding_raises_on_status(L):
     with pytest.raises(mx.MXNormError) as ei:
         mx.mxnorm_quant_fwd(FAKE, 8, 48, 2, 0, FAKE, FAKE, FAKE)
