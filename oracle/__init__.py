@@ -79,6 +79,8 @@ def _load():
     lib.oracle_h32_groups.argtypes = [p, i64, p]
     lib.oracle_float_to_bf16_array.argtypes = [p, i64, p]
     lib.oracle_mxnorm_bwd_ste_rows.argtypes = [p, p, p, i64, i64, p, p]
+    lib.oracle_nvfp4_rows.argtypes = [p, i64, i64, i32, f32, p, p, p]
+    lib.oracle_nvfp4_rows.restype = i32
     lib.oracle_mxnorm_bwd_ste_rows.restype = i32
     lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
     lib.oracle_decode_e4m3.restype = ctypes.c_double
@@ -154,6 +156,20 @@ def rmsnorm_mxfp8(x_bits: np.ndarray, eps: float = 1e-5):
     if lib.oracle_rmsnorm_mxfp8_rows(_ptr(x), T, H, float(eps), _ptr(y), _ptr(codes), _ptr(scales), _ptr(inv)) != 0:
         raise ValueError("oracle rejected arguments")
     return y, codes, scales, inv
+
+
+def nvfp4_quant(x_bits: np.ndarray, p: int, tensor_scale: float):
+    """NVFP4 forward (16-element blocks, UE4M3 block scales over a tensor
+    scale g): (codes u8 [T, H/2], scales u8 [T, H/16], inv_rms f32 [T])."""
+    lib = _load()
+    x = _as_bf16_bits(x_bits)
+    T, H = x.shape
+    codes = np.empty((T, H // 2), np.uint8)
+    scales = np.empty((T, H // 16), np.uint8)
+    inv = np.empty((T,), np.float32)
+    if lib.oracle_nvfp4_rows(_ptr(x), T, H, int(p), float(tensor_scale), _ptr(codes), _ptr(scales), _ptr(inv)) != 0:
+        raise ValueError("oracle rejected arguments")
+    return codes, scales, inv
 
 
 def mxnorm_bwd_ste(x_bits: np.ndarray, dy_bits: np.ndarray, inv_rms: np.ndarray, with_f64: bool = False):

@@ -219,3 +219,32 @@ def _round_inv_power_mean(mean: Fraction, p: int) -> Fraction:
             raise ArithmeticError("exact tie in sqrt rounding cannot happen for these inputs")
         f = round_to_fp32(f + ulp) if target >= hi_mid * hi_mid else round_to_fp32(f - ulp)
     raise ArithmeticError("fp32 rounding of 1/sqrt did not settle")
+
+
+# ------------------------------------------------------------------ NVFP4
+def nvfp4_row(bits_row, p: int, g_bits: int):
+    """NVFP4 of one finite bf16 row with tensor scale g (fp32 bit pattern):
+    (code bytes, UE4M3 scale codes, inv_rms as an exact fp32 value or None
+    for +Inf).  Every fp32 operation is an exact rational rounded by
+    round_to_fp32; the block-scale cast scans all E4M3 codes."""
+    g = fp32_value(g_bits)
+    H = len(bits_row)
+    assert H % 16 == 0
+    K = H // 16
+    sixg = round_to_fp32(6 * g)
+    codes, scales, ssum = [], [], Fraction(0)
+    for k in range(K):
+        vals = [bf16_value(b) for b in bits_row[16 * k:16 * k + 16]]
+        signs = [b >> 15 for b in bits_row[16 * k:16 * k + 16]]
+        amax = max(abs(v) for v in vals)
+        sb = round_to_fp32(amax / sixg)
+        sc = nearest_code(sb, _E4M3, 0)
+        scales.append(sc)
+        sval = _E4M3[sc]
+        enc = Fraction(0) if sval == 0 else round_to_fp32(1 / round_to_fp32(sval * g))
+        nib = [nearest_code(round_to_fp32(v * enc), _E2M1, sgn) for v, sgn in zip(vals, signs)]
+        codes.extend(nib[j] | (nib[j + 1] << 4) for j in range(0, 16, 2))
+        ssum += (sval * g) ** p
+    if ssum == 0:
+        return codes, scales, None
+    return codes, scales, _round_inv_power_mean(ssum / K, p)

@@ -44,6 +44,15 @@
  *   - E2M1 packing: element 2i in the low nibble of byte i.
  *   - RMSNorm baseline: inv = RN_fp32(1/sqrt(mean(x^2) + eps)),
  *     y = RN_bf16(RN_fp32(x * inv)), then the MXFP8 cast of y.
+ *   - NVFP4 variant (the pages quote its layer speedup but not the format):
+ *     16-element blocks, E2M1 elements, a UE4M3 block scale and a caller-
+ *     given fp32 tensor scale g > 0.  Per block, in fp32: sixg = RN(6 g),
+ *     sb = RN(amax / sixg), s = sat_RNE_E4M3(sb) (positive), d = RN(s g),
+ *     enc = RN(1 / d) (0 when s = 0), r_j = RN(x_j * enc), codes =
+ *     sat_RNE_E2M1(r_j).  The estimator's m~_k is the block's decode scale
+ *     s_k * g; inv_rms = ((1/K) sum_k (s_k g)^p)^(-1/p), K = H/16, +Inf when
+ *     every s_k is 0.  A block with Inf/NaN: scale code 0x7F, codes 0, row
+ *     inv_rms NaN.
  *   - Backward (straight-through estimator, [MXN] section 2, "Gradientes":
  *     RMSNorm's gradient logic reused, nothing saved but the normaliser):
  *     the cast is treated as the identity and RMSNorm's backward runs with
@@ -436,6 +445,64 @@ int oracle_rmsnorm_mxfp8_rows(const uint16_t *x, int64_t T, int64_t H, float eps
         }
     }
     return oracle_mx_cast_rows(y, T, H, OR_FMT_MXFP8_E4M3, codes, scales);
+}
+
+/* --------------------------------------------------------------- NVFP4 */
+
+/* Value of a non-negative E4M3 code (its magnitude bits). */
+static double e4m3_code_value(uint8_t c)
+{
+    return e4m3_value(c & 0x7F);
+}
+
+/* NVFP4 forward of T rows (see the header comment): codes [T, H/2] (element
+ * 2i in the low nibble), scales [T, H/16] (UE4M3 codes), inv_rms [T]. */
+int oracle_nvfp4_rows(const uint16_t *x, int64_t T, int64_t H, int p, float g,
+                      uint8_t *codes, uint8_t *scales, float *inv_rms)
+{
+    if (T < 0 || H <= 0 || H % 16 != 0 || (p != 1 && p != 2) || !(g > 0.0f) || !isfinite(g)) return 1;
+    const int64_t K = H / 16;
+    const float sixg = 6.0f * g;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t *row = x + t * H;
+        double sum = 0.0;
+        int row_finite = 1;
+        for (int64_t k = 0; k < K; ++k) {
+            double amax = 0.0;
+            int finite = 1;
+            for (int j = 0; j < 16; ++j) {
+                double v = (double)bf16_bits_to_float(row[k * 16 + j]);
+                if (!isfinite(v)) finite = 0;
+                else if (fabs(v) > amax) amax = fabs(v);
+            }
+            uint8_t *crow = codes + t * (H / 2) + k * 8;
+            if (!finite) {
+                scales[t * K + k] = 0x7F;
+                for (int j = 0; j < 8; ++j) crow[j] = 0;
+                row_finite = 0;
+                continue;
+            }
+            const float sb = (float)amax / sixg;
+            const uint8_t sc = oracle_cast_e4m3((double)sb);
+            scales[t * K + k] = sc;
+            const float sval = (float)e4m3_code_value(sc);
+            const float d = sval * g;
+            const float enc = (sval == 0.0f) ? 0.0f : 1.0f / d;
+            for (int j = 0; j < 16; j += 2) {
+                const float r0 = bf16_bits_to_float(row[k * 16 + j]) * enc;
+                const float r1 = bf16_bits_to_float(row[k * 16 + j + 1]) * enc;
+                crow[j / 2] = (uint8_t)(oracle_cast_e2m1((double)r0) | (oracle_cast_e2m1((double)r1) << 4));
+            }
+            const double m = (double)sval * (double)g;      /* m~_k = s_k g */
+            sum += (p == 1) ? m : m * m;
+        }
+        if (!row_finite) { inv_rms[t] = NAN; continue; }
+        if (sum == 0.0) { inv_rms[t] = INFINITY; continue; }
+        const double mean = sum / (double)K;
+        const double m_p = (p == 1) ? mean : sqrt(mean);
+        inv_rms[t] = (float)(1.0 / m_p);
+    }
+    return 0;
 }
 
 /* ------------------------------------------------------------ backward */

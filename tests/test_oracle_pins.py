@@ -483,3 +483,61 @@ def test_bwd_closed_forms(oracle_mod):
     want0 = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits((0.75 * synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(dy[0]))).astype(np.float32)))
     np.testing.assert_array_equal(dx[0], want0)
     assert np.abs(dx[1]).max() <= 1e-6
+
+
+# ------------------------------------------------------------------ NVFP4
+def _f32_bits(v):
+    import struct
+    return struct.unpack("<I", struct.pack("<f", float(np.float32(v))))[0]
+
+
+@pytest.mark.parametrize("g", [1.0, 0.0123, 3.7e-3, 2.5e-5])
+@pytest.mark.parametrize("p", [1, 2])
+def test_nvfp4_vs_bruteforce(oracle_mod, g, p):
+    from oracle import bruteforce as bf
+    rng = np.random.default_rng(int(g * 1e6) + p)
+    x = rng.standard_normal((4, 64)).astype(np.float32) * np.float32(3.0)
+    x[1, 5] *= 200
+    x[2, :16] *= 1e-6       # a block whose scale underflows for large g
+    xb = synth.f32_to_bf16_bits(x)
+    gf = float(np.float32(g))
+    c, s, i = oracle_mod.nvfp4_quant(xb, p, gf)
+    for t in range(4):
+        bc, bs, bi = bf.nvfp4_row([int(v) for v in xb[t]], p, _f32_bits(gf))
+        assert list(c[t]) == bc and list(s[t]) == bs
+        assert (bi is None and np.isinf(i[t])) or Fraction(float(i[t])) == bi
+
+
+def test_nvfp4_closed_forms(oracle_mod):
+    """Constant row 6.0 with g = 1: block scale 6/6 = 1.0 (E4M3 0x38), codes
+    6.0 (0x7 | 0x7 << 4), inv_rms = 1/(1 * 1) = 1.  A zero row: scales 0,
+    codes 0, inv_rms +Inf.  A block beyond 448 * 6 * g saturates its scale
+    at 448 (0x7E) and its codes at 6."""
+    x = synth.f32_to_bf16_bits(np.full((1, 32), 6.0, np.float32))
+    c, s, i = oracle_mod.nvfp4_quant(x, 2, 1.0)
+    assert (s == 0x38).all() and (c == 0x77).all() and i[0] == 1.0
+    c, s, i = oracle_mod.nvfp4_quant(np.zeros((1, 32), np.uint16), 2, 1.0)
+    assert (s == 0).all() and (c == 0).all() and np.isinf(i[0])
+    x = synth.f32_to_bf16_bits(np.full((1, 16), 5000.0, np.float32))
+    c, s, i = oracle_mod.nvfp4_quant(x, 1, 1.0)
+    assert (s == 0x7E).all() and (c == 0x77).all()
+    assert i[0] == np.float32(1.0 / 448.0)
+
+
+def test_nvfp4_invariants(oracle_mod):
+    """Decoded values never exceed 6 * s * g, the block scale is the E4M3
+    rounding of amax / (6 g), and the p = 2 estimate is the quadratic mean of
+    the decode scales."""
+    w = synth.WORKLOADS["llama3_8b_65536x4096"]
+    x = synth.make_activations(w, rows=4)
+    xv = synth.bf16_bits_to_f32(x).astype(np.float64)
+    g = float(np.float32(np.abs(xv).max() / (448 * 6)))
+    c, s, i = oracle_mod.nvfp4_quant(x, 2, g)
+    sval = np.vectorize(oracle_mod.decode_e4m3)(s)
+    amax = np.abs(xv).reshape(4, -1, 16).max(-1)
+    np.testing.assert_array_equal(s, oracle_mod.cast_e4m3((amax.astype(np.float32) / np.float32(6 * np.float32(g))).astype(np.float64)))
+    nib = np.stack([c & 0xF, c >> 4], -1).reshape(4, -1)
+    dec = np.vectorize(oracle_mod.decode_e2m1)(nib).reshape(4, -1, 16)
+    assert (np.abs(dec) <= 6).all()
+    want = 1.0 / np.sqrt(((sval * g) ** 2).mean(1))
+    np.testing.assert_allclose(i, want, rtol=1e-6)
