@@ -261,6 +261,24 @@ def run_gpu(args):
                                "bytes_per_row": 6 * H + 4}
     del dy, dxs
 
+    # NVFP4 (16-element blocks, UE4M3 scales, tensor scale from amax / (448*6))
+    g = mx.nvfp4_tensor_scale(xs[0])
+    c4n = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
+    s4n = torch.empty((T, H // 16), dtype=torch.uint8, device=dev)
+
+    def nvfp4_step(i):
+        st = mx.lib().mxnorm_quant_fwd_nvfp4(xs[i].data_ptr(), T, H, 2, ctypes.c_float(g), c4n.data_ptr(),
+                                             s4n.data_ptr(), outs[i][2].data_ptr(), ctypes.c_void_p(sptr))
+        if st:
+            raise RuntimeError(mx.lib().mxnorm_last_error().decode())
+
+    pern, _ = time_launches(torch, stream, nvfp4_step, sec_steps, 5, nbuf)
+    m = statistics.fmean(pern)
+    bn = T * (2 * H + H // 2 + H // 16 + 4)
+    extra["mxnorm_nvfp4_p2"] = {"ms": round(m, 5), "GB/s": gbs(bn, m), "frac": round(gbs(bn, m) / hbm_peak, 4),
+                                "bytes_per_row": 2 * H + H // 2 + H // 16 + 4}
+    del c4n, s4n
+
     y_ws = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
 
     def base_step(i):

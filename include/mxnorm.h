@@ -124,6 +124,30 @@ int mxnorm_quant_fwd_ex(const void* x, int64_t T, int64_t H, int p, int fmt, voi
 int rmsnorm_mxfp8_ref_fwd(const void* x, int64_t T, int64_t H, float eps, void* y_workspace,
                           uint8_t* codes, uint8_t* scales, float* inv_rms, void* stream);
 
+/* MXNorm over the NVFP4 cast.  The pages quote its Llama 3 8B layer speedup
+ * ("MXNorm ...", Resumen tecnico, section 4, Rendimiento) without the
+ * format; the recipe here: 16-element blocks of FP4 E2M1 values, one UE4M3
+ * scale per block, an fp32 tensor scale g > 0 given by the caller (e.g.
+ * amax / (448 * 6) from mxnorm_absmax_bf16).  Per block, in fp32 with IEEE
+ * rounding: sb = amax / (6 g); s = E4M3(sb) saturating RNE; d = s g;
+ * enc = 1 / d (0 when s = 0); codes = E2M1(x * enc) saturating RNE, sign
+ * kept, element 2i in the low nibble.  The estimator takes the decode scales
+ * s_k g:  inv_rms = ((1/K) sum_k (s_k g)^p)^(-1/p), K = H/16; +Inf for an
+ * all-zero row.  A block holding Inf/NaN gets scale 0x7F, codes 0, and its
+ * row's inv_rms is NaN.
+ *   x        bf16  [T, H], H % 16 == 0   16-byte aligned
+ *   codes    uint8 [T, H/2]              16-byte aligned
+ *   scales   uint8 [T, H/16] (UE4M3)
+ *   inv_rms  f32   [T]                   4-byte aligned
+ * Errors as mxnorm_quant_fwd (a non-finite or non-positive tensor_scale is
+ * MXNORM_ERR_INVALID_ARG). */
+int mxnorm_quant_fwd_nvfp4(const void* x, int64_t T, int64_t H, int p, float tensor_scale, void* codes,
+                           uint8_t* scales, float* inv_rms, void* stream);
+
+/* max |x| over n bf16 values, written as an fp32 to the device pointer amax
+ * (NaN if any x is NaN).  Zeroes *amax first on the same stream. */
+int mxnorm_absmax_bf16(const void* x, int64_t n, float* amax, void* stream);
+
 /* Straight-through backward of MXNorm ("MXNorm ...", Resumen tecnico,
  * 2. Metodologia, "Gradientes": RMSNorm's gradient logic reused through a
  * straight-through estimator, nothing kept but what RMSNorm keeps).  The MX

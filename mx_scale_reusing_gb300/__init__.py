@@ -19,7 +19,7 @@ import os
 __all__ = [
     "FMT", "VARIANT", "MXNormError", "MXNormLibraryMissing", "lib", "library_path",
     "mxnorm_quant_fwd", "quant_fwd", "quant_fwd_host", "rmsnorm_mxfp8_ref_fwd", "device_errors",
-    "code_bytes", "bwd_ste",
+    "code_bytes", "bwd_ste", "quant_fwd_nvfp4", "absmax", "nvfp4_tensor_scale",
 ]
 
 FMT = {"mxfp8": 0, "mxfp4": 1, "mxfp4_h16": 2, "mxfp8_h16": 3, "mxfp4_h32": 4, "mxfp8_h32": 5}
@@ -63,6 +63,10 @@ def lib() -> ctypes.CDLL:
     L.mxnorm_last_error.argtypes = []
     L.mxnorm_last_error.restype = ctypes.c_char_p
     L.mxnorm_abi_version.restype = i32
+    L.mxnorm_quant_fwd_nvfp4.argtypes = [vp, i64, i64, i32, ctypes.c_float, vp, vp, vp, vp]
+    L.mxnorm_quant_fwd_nvfp4.restype = i32
+    L.mxnorm_absmax_bf16.argtypes = [vp, i64, vp, vp]
+    L.mxnorm_absmax_bf16.restype = i32
     L.mxnorm_bwd_ste.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     L.mxnorm_bwd_ste.restype = i32
     L.mxnorm_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
@@ -137,6 +141,47 @@ def rmsnorm_mxfp8_ref_fwd(x, eps: float = 1e-5, out=None, stream=None):
     _check(lib().rmsnorm_mxfp8_ref_fwd(x.data_ptr(), T, H, float(eps), y.data_ptr(), codes.data_ptr(),
                                        scales.data_ptr(), inv.data_ptr(), _stream_ptr(x.device, stream)))
     return y, codes, scales, inv
+
+
+def absmax(x, stream=None):
+    """max |x| of a contiguous bf16 CUDA tensor, as a 1-element float32 CUDA
+    tensor (asynchronous)."""
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous bfloat16 CUDA tensor")
+    out = torch.empty((1,), dtype=torch.float32, device=x.device)
+    _check(lib().mxnorm_absmax_bf16(x.data_ptr(), x.numel(), out.data_ptr(), _stream_ptr(x.device, stream)))
+    return out
+
+
+def nvfp4_tensor_scale(x) -> float:
+    """The usual NVFP4 tensor scale amax(x) / (448 * 6) (fp32; 1.0 for an
+    all-zero tensor).  Synchronises to read amax."""
+    import numpy as np
+    a = np.float32(absmax(x).item())
+    return float(a / np.float32(2688.0)) if a > 0 else 1.0
+
+
+def quant_fwd_nvfp4(x, p: int = 2, tensor_scale=None, out=None, stream=None):
+    """MXNorm over the NVFP4 cast of a contiguous bf16 CUDA tensor [..., H]
+    (H % 16 == 0).  Returns (codes uint8 [..., H/2], scales uint8 [..., H/16]
+    UE4M3, inv_rms float32 [...]).  tensor_scale defaults to
+    nvfp4_tensor_scale(x)."""
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous bfloat16 CUDA tensor")
+    H = x.shape[-1]
+    T = x.numel() // H if H else 0
+    lead = tuple(x.shape[:-1])
+    g = nvfp4_tensor_scale(x) if tensor_scale is None else float(tensor_scale)
+    if out is None:
+        out = (torch.empty(lead + (H // 2,), dtype=torch.uint8, device=x.device),
+               torch.empty(lead + (H // 16,), dtype=torch.uint8, device=x.device),
+               torch.empty(lead, dtype=torch.float32, device=x.device))
+    codes, scales, inv = out
+    _check(lib().mxnorm_quant_fwd_nvfp4(x.data_ptr(), T, H, int(p), g, codes.data_ptr(), scales.data_ptr(),
+                                        inv.data_ptr(), _stream_ptr(x.device, stream)))
+    return codes, scales, inv
 
 
 def bwd_ste(x, dy, inv_rms, out=None, stream=None):

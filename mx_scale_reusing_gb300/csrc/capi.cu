@@ -144,6 +144,37 @@ int mxnorm_bwd_ste(const void* x, const void* dy, const float* inv_rms, int64_t 
   return MXNORM_OK;
 }
 
+int mxnorm_quant_fwd_nvfp4(const void* x, int64_t T, int64_t H, int p, float tensor_scale, void* codes,
+                           uint8_t* scales, float* inv_rms, void* stream) {
+  g_last_error.clear();
+  if (p != 1 && p != 2) return fail(MXNORM_ERR_INVALID_ARG, "p = %d is not 1 or 2", p);
+  if (!(tensor_scale > 0.0f) || !(tensor_scale < 3.4028235e38f))
+    return fail(MXNORM_ERR_INVALID_ARG, "tensor_scale must be a finite positive float");
+  if (T < 0) return fail(MXNORM_ERR_INVALID_ARG, "T = %lld < 0", (long long)T);
+  if (H <= 0 || H % 16 != 0)
+    return fail(MXNORM_ERR_INVALID_ARG, "H = %lld is not a positive multiple of 16", (long long)H);
+  if (H > MXNORM_MAX_H)
+    return fail(MXNORM_ERR_UNSUPPORTED, "H = %lld exceeds MXNORM_MAX_H = %d", (long long)H, MXNORM_MAX_H);
+  if (T == 0) return MXNORM_OK;
+  if (!x || !codes || !scales || !inv_rms) return fail(MXNORM_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(x, 16) || !aligned(codes, 16)) return fail(MXNORM_ERR_MISALIGNED, "x and codes need 16-byte alignment");
+  if (!aligned(inv_rms, 4)) return fail(MXNORM_ERR_MISALIGNED, "inv_rms is not 4-byte aligned");
+  cudaError_t err = launch_nvfp4(Nvfp4Args{x, T, H, p, tensor_scale, codes, scales, inv_rms},
+                                 static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "mxnorm_quant_fwd_nvfp4 launch");
+  return MXNORM_OK;
+}
+
+int mxnorm_absmax_bf16(const void* x, int64_t n, float* amax, void* stream) {
+  g_last_error.clear();
+  if (n < 0) return fail(MXNORM_ERR_INVALID_ARG, "n < 0");
+  if (!amax || (n > 0 && !x)) return fail(MXNORM_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(amax, 4) || !aligned(x, 2)) return fail(MXNORM_ERR_MISALIGNED, "amax needs 4-byte, x 2-byte alignment");
+  cudaError_t err = launch_absmax_bf16(x, n, amax, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "mxnorm_absmax_bf16 launch");
+  return MXNORM_OK;
+}
+
 const char* mxnorm_status_string(int status) {
   switch (status) {
     case MXNORM_OK: return "MXNORM_OK";

@@ -36,6 +36,17 @@ struct BwdArgs {
   void* dx;            // bf16 [T, H]
 };
 
+struct Nvfp4Args {
+  const void* x;       // bf16 [T, H], H % 16 == 0
+  int64_t T;
+  int64_t H;
+  int p;
+  float g;             // fp32 tensor scale (> 0, finite)
+  void* codes;         // u8 [T, H/2]
+  uint8_t* scales;     // UE4M3 [T, H/16]
+  float* inv_rms;      // f32 [T]
+};
+
 struct TiledArgs {
   WarpRowArgs base;
   unsigned int* error_flag;  // device word set when a bounded wait gives up
@@ -52,6 +63,8 @@ cudaError_t launch_rmsnorm_bf16(const RmsNormArgs& a, cudaStream_t s);
 cudaError_t launch_mxnorm_tiled(const TiledArgs& a, cudaStream_t s);
 bool tiled_supported(int64_t H, int fmt);
 cudaError_t launch_mxnorm_bwd_ste(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_nvfp4(const Nvfp4Args& a, cudaStream_t s);
+cudaError_t launch_absmax_bf16(const void* x, int64_t n, float* amax, cudaStream_t s);
 
 // Replace the calling thread's message returned by mxnorm_last_error().
 void set_last_error(const char* msg);

@@ -86,6 +86,19 @@ def test_bwd_validation(L):
     assert L.mxnorm_bwd_ste(FAKE, FAKE, FAKE, 8, (1 << 20) + 32, FAKE, None) == 2
 
 
+def test_nvfp4_validation(L):
+    q = L.mxnorm_quant_fwd_nvfp4
+    assert q(FAKE, 0, 4096, 2, 1.0, FAKE, FAKE, FAKE, None) == 0
+    assert q(FAKE, 8, 4096, 3, 1.0, FAKE, FAKE, FAKE, None) == 1
+    assert q(FAKE, 8, 4096, 2, 0.0, FAKE, FAKE, FAKE, None) == 1
+    assert q(FAKE, 8, 4096, 2, float("inf"), FAKE, FAKE, FAKE, None) == 1
+    assert q(FAKE, 8, 4096, 2, float("nan"), FAKE, FAKE, FAKE, None) == 1
+    assert q(FAKE, 8, 24, 2, 1.0, FAKE, FAKE, FAKE, None) == 1
+    assert q(FAKE, 8, 48, 2, 1.0, FAKE + 8, FAKE, FAKE, None) == 3
+    assert L.mxnorm_absmax_bf16(FAKE, -1, FAKE, None) == 1
+    assert L.mxnorm_absmax_bf16(FAKE, 8, None, None) == 1
+
+
 def test_python_binding_raises_on_status(L):
     with pytest.raises(mx.MXNormError) as ei:
         mx.mxnorm_quant_fwd(FAKE, 8, 48, 2, 0, FAKE, FAKE, FAKE)
