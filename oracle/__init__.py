@@ -80,6 +80,8 @@ def _load():
     lib.oracle_float_to_bf16_array.argtypes = [p, i64, p]
     lib.oracle_mxnorm_bwd_ste_rows.argtypes = [p, p, p, i64, i64, p, p]
     lib.oracle_nvfp4_rows.argtypes = [p, i64, i64, i32, f32, p, p, p]
+    lib.oracle_mxfp8_linear.argtypes = [p, p, p, p, p, i64, i64, i64, p]
+    lib.oracle_mxfp8_linear.restype = i32
     lib.oracle_nvfp4_rows.restype = i32
     lib.oracle_mxnorm_bwd_ste_rows.restype = i32
     lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
@@ -156,6 +158,25 @@ def rmsnorm_mxfp8(x_bits: np.ndarray, eps: float = 1e-5):
     if lib.oracle_rmsnorm_mxfp8_rows(_ptr(x), T, H, float(eps), _ptr(y), _ptr(codes), _ptr(scales), _ptr(inv)) != 0:
         raise ValueError("oracle rejected arguments")
     return y, codes, scales, inv
+
+
+def mxfp8_linear(x_codes, x_scales, inv_rms, w_codes, w_scales) -> np.ndarray:
+    """out[t, n] = inv_rms[t] * sum_k xv[t, k] wv[n, k] in fp64 (MXNormLinear's
+    consumer GEMM with the gain folded into w); scales row-major [rows, K/32]."""
+    lib = _load()
+    xc = np.ascontiguousarray(x_codes, np.uint8)
+    wc = np.ascontiguousarray(w_codes, np.uint8)
+    xs = np.ascontiguousarray(x_scales, np.uint8)
+    ws = np.ascontiguousarray(w_scales, np.uint8)
+    inv = np.ascontiguousarray(inv_rms, np.float32)
+    T, K = xc.shape
+    N = wc.shape[0]
+    if wc.shape[1] != K or xs.shape != (T, K // BLOCK) or ws.shape != (N, K // BLOCK) or inv.shape != (T,):
+        raise ValueError("shape mismatch")
+    out = np.empty((T, N), np.float64)
+    if lib.oracle_mxfp8_linear(_ptr(xc), _ptr(xs), _ptr(inv), _ptr(wc), _ptr(ws), T, K, N, _ptr(out)) != 0:
+        raise ValueError("oracle rejected arguments")
+    return out
 
 
 def nvfp4_quant(x_bits: np.ndarray, p: int, tensor_scale: float):

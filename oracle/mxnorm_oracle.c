@@ -505,6 +505,32 @@ int oracle_nvfp4_rows(const uint16_t *x, int64_t T, int64_t H, int p, float g,
     return 0;
 }
 
+/* ------------------------------------------------------- MXNormLinear */
+
+/* Consumer side of MXNormLinear ([MXN] section 2, Implementacion: the gain
+ * is folded into the next layer's weight, the row scale commutes with the
+ * matmul): out[t][n] = inv_rms[t] * sum_k xv[t][k] * wv[n][k], where xv / wv
+ * are E4M3 code values times their E8M0 block scales (32 elements along K,
+ * row-major scale arrays [rows][K/32]).  fp64, every product exact. */
+int oracle_mxfp8_linear(const uint8_t *xc, const uint8_t *xs, const float *inv_rms, const uint8_t *wc,
+                        const uint8_t *ws, int64_t T, int64_t K, int64_t N, double *out)
+{
+    if (T < 0 || K <= 0 || K % OR_BLOCK != 0 || N <= 0) return 1;
+    const int64_t KB = K / OR_BLOCK;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double xv = ldexp(oracle_decode_e4m3(xc[t * K + k]), (int)xs[t * KB + k / OR_BLOCK] - 127);
+                const double wv = ldexp(oracle_decode_e4m3(wc[n * K + k]), (int)ws[n * KB + k / OR_BLOCK] - 127);
+                acc += xv * wv;
+            }
+            out[t * N + n] = (double)inv_rms[t] * acc;
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------ backward */
 
 /* Straight-through backward of T rows: x, dy bf16 [T, H], inv_rms [T] (the

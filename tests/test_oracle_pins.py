@@ -541,3 +541,41 @@ def test_nvfp4_invariants(oracle_mod):
     assert (np.abs(dec) <= 6).all()
     want = 1.0 / np.sqrt(((sval * g) ** 2).mean(1))
     np.testing.assert_allclose(i, want, rtol=1e-6)
+
+
+# ---------------------------------------------------------- MXNormLinear
+def _e4m3_values(codes):
+    from oracle import bruteforce as bf
+    table = np.full(256, np.nan)
+    for c, v in bf.e4m3_values().items():
+        table[c] = float(v)
+    return table[codes]
+
+
+def test_linear_matches_matmul_of_dequantized(oracle_mod):
+    """The consumer GEMM equals diag(inv) @ (Xv @ Wv^T) with numpy's matmul on
+    the dequantised operands (E4M3 values from the brute-force code table
+    times 2^(scale - 127))."""
+    x = synth.make_activations(synth.WORKLOADS["llama3_125m_16384x768"], rows=8)
+    xc, xs, inv = oracle_mod.mxnorm_quant(x, 2, "mxfp8")
+    w = synth.make_random_rows(24, 768, seed=3, scale=0.05)
+    wc, ws = oracle_mod.mx_cast(w, "mxfp8")
+    xv = _e4m3_values(xc) * np.repeat(np.exp2(xs.astype(np.float64) - 127), 32, axis=1)
+    wv = _e4m3_values(wc) * np.repeat(np.exp2(ws.astype(np.float64) - 127), 32, axis=1)
+    want = inv.astype(np.float64)[:, None] * (xv @ wv.T)
+    got = oracle_mod.mxfp8_linear(xc, xs, inv, wc, ws)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-300)
+
+
+def test_linear_identity_weight(oracle_mod):
+    """W^ = identity (code 1.0, scale 2^0): out = inv * x^."""
+    K = 64
+    xc = np.array([[0x38 + (k % 7) for k in range(K)], [0xB0 + (k % 5) for k in range(K)]], np.uint8)
+    xs = np.array([[120, 130], [127, 100]], np.uint8)
+    inv = np.array([0.5, 3.0], np.float32)
+    wc = np.zeros((K, K), np.uint8)
+    wc[np.arange(K), np.arange(K)] = 0x38
+    ws = np.full((K, K // 32), 127, np.uint8)
+    got = oracle_mod.mxfp8_linear(xc, xs, inv, wc, ws)
+    xv = _e4m3_values(xc) * np.repeat(np.exp2(xs.astype(np.float64) - 127), 32, axis=1)
+    np.testing.assert_array_equal(got, inv.astype(np.float64)[:, None] * xv)
