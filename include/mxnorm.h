@@ -102,6 +102,20 @@ typedef enum {
                                     async copies (TMA engine), persistent CTAs */
 } mxnorm_variant;
 
+/* Layouts of the E8M0 scales a call writes or reads. */
+#define MXNORM_SCALE_ROW_MAJOR 0   /* scales[row * (H/32) + k]                          */
+#define MXNORM_SCALE_MMA 1         /* the 512-byte atoms the block-scaled tensor-core MMA
+                                    * reads (H % 128 == 0): one atom per 128 rows x 4
+                                    * blocks, atoms ordered (row tile, block group) with
+                                    * the block group fastest; inside an atom the byte of
+                                    * (r, k) is at (r % 32) * 16 + ((r / 32) % 4) * 4 + k % 4.
+                                    * Rows are padded to a multiple of 128: the buffer
+                                    * holds mxnorm_mma_scale_bytes(T, H) bytes, and the
+                                    * bytes of padding rows are unspecified. */
+
+/* Bytes of an MXNORM_SCALE_MMA scale buffer for rows x H (-1 if H % 128 != 0). */
+int64_t mxnorm_mma_scale_bytes(int64_t rows, int64_t H);
+
 /* MXNorm forward: MX codes + E8M0 scales + fp32 inverse-RMS estimate of
  * every row of x, in one pass over x (the estimator of "Fundamentos
  * Teoricos" evaluated on the scales of the cast, see above).
@@ -113,6 +127,40 @@ int mxnorm_quant_fwd(const void* x, int64_t T, int64_t H, int p, int fmt, void* 
  * Every variant writes bit-identical outputs. */
 int mxnorm_quant_fwd_ex(const void* x, int64_t T, int64_t H, int p, int fmt, void* codes,
                         uint8_t* scales, float* inv_rms, int variant, void* stream);
+
+/* As mxnorm_quant_fwd (variant AUTO) with the scales written in
+ * scale_layout (MXNORM_SCALE_ROW_MAJOR or MXNORM_SCALE_MMA); the MMA layout
+ * feeds mxnorm_linear_fwd without a conversion pass. */
+int mxnorm_quant_fwd_layout(const void* x, int64_t T, int64_t H, int p, int fmt, void* codes, uint8_t* scales,
+                            float* inv_rms, int scale_layout, void* stream);
+
+/* The MX cast alone (no estimator) of T rows of H bf16 values: MXFP8 E4M3
+ * codes [T, H] and E8M0 scales in scale_layout.  Used for the consumer
+ * weight of MXNormLinear: pass the rows of W'^T (one per output feature,
+ * W' = diag(c * gamma) W) to get the w_codes / w_scales of
+ * mxnorm_linear_fwd.  fmt must be MXNORM_FMT_MXFP8_E4M3. */
+int mx_cast_fwd(const void* x, int64_t T, int64_t H, int fmt, void* codes, uint8_t* scales, int scale_layout,
+                void* stream);
+
+/* Consumer side of MXNormLinear ("MXNorm ...", Resumen tecnico, 2.
+ * Metodologia, "Implementacion": the gain is folded into the next linear
+ * layer's weight): an MXFP8 block-scaled GEMM on the tensor cores whose
+ * epilogue applies the row's inverse RMS,
+ *     out[t, n] = bf16( inv_rms[t] * sum_k x^[t, k] * w^[n, k] ),
+ * x^ / w^ the values of the E4M3 codes times their E8M0 block scales (32
+ * elements along K), accumulated in fp32, the product with inv_rms rounded
+ * to fp32 and then to bf16.
+ *   x_codes   E4M3 [T, K]                 16-byte aligned
+ *   x_scales  E8M0, MXNORM_SCALE_MMA      mxnorm_mma_scale_bytes(T, K) bytes
+ *   inv_rms   f32  [T]                    e.g. from mxnorm_quant_fwd_layout
+ *   w_codes   E4M3 [N, K]                 16-byte aligned
+ *   w_scales  E8M0, MXNORM_SCALE_MMA      mxnorm_mma_scale_bytes(N, K) bytes
+ *   out       bf16 [T, N]                 16-byte aligned
+ * K % 128 == 0, N % 256 == 0, any T.  Errors and stream semantics as
+ * mxnorm_quant_fwd; bit 1 of mxnorm_device_errors reports a timed-out
+ * pipeline wait of this kernel. */
+int mxnorm_linear_fwd(const void* x_codes, const uint8_t* x_scales, const float* inv_rms, const void* w_codes,
+                      const uint8_t* w_scales, int64_t T, int64_t K, int64_t N, void* out, void* stream);
 
 /* Two-pass baseline: the unfused pipeline MXNorm replaces ("MXNorm ...",
  * Resumen tecnico, section 1: RMSNorm and the MXFP8 cast as separate
@@ -198,7 +246,8 @@ int mxnorm_abi_version(void);
 
 /* Device-side error word of the current device, or'ed by kernels whose
  * bounded waits gave up (bit 0: a shared-memory pipeline wait of the tiled
- * variant timed out; its outputs for the affected rows are then invalid).
+ * variant timed out; bit 1: one of mxnorm_linear_fwd; the outputs of the
+ * affected call are then invalid).
  * Synchronous: copies the word to *flags (and zeroes it when clear != 0).
  * Call after the work in question has completed. */
 int mxnorm_device_errors(uint32_t* flags, int clear);

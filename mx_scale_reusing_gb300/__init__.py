@@ -19,7 +19,8 @@ import os
 __all__ = [
     "FMT", "VARIANT", "MXNormError", "MXNormLibraryMissing", "lib", "library_path",
     "mxnorm_quant_fwd", "quant_fwd", "quant_fwd_host", "rmsnorm_mxfp8_ref_fwd", "device_errors",
-    "code_bytes", "bwd_ste", "quant_fwd_nvfp4", "absmax", "nvfp4_tensor_scale",
+    "code_bytes", "bwd_ste", "quant_fwd_nvfp4", "absmax", "nvfp4_tensor_scale", "quant_fwd_mma", "mx_cast",
+    "linear_fwd", "mma_scale_bytes",
 ]
 
 FMT = {"mxfp8": 0, "mxfp4": 1, "mxfp4_h16": 2, "mxfp8_h16": 3, "mxfp4_h32": 4, "mxfp8_h32": 5}
@@ -68,6 +69,14 @@ def lib() -> ctypes.CDLL:
     L.mxnorm_absmax_bf16.argtypes = [vp, i64, vp, vp]
     L.mxnorm_absmax_bf16.restype = i32
     L.mxnorm_bwd_ste.argtypes = [vp, vp, vp, i64, i64, vp, vp]
+    L.mxnorm_mma_scale_bytes.argtypes = [i64, i64]
+    L.mxnorm_mma_scale_bytes.restype = i64
+    L.mxnorm_quant_fwd_layout.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp, i32, vp]
+    L.mxnorm_quant_fwd_layout.restype = i32
+    L.mx_cast_fwd.argtypes = [vp, i64, i64, i32, vp, vp, i32, vp]
+    L.mx_cast_fwd.restype = i32
+    L.mxnorm_linear_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]
+    L.mxnorm_linear_fwd.restype = i32
     L.mxnorm_bwd_ste.restype = i32
     L.mxnorm_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     L.mxnorm_device_errors.restype = i32
@@ -182,6 +191,67 @@ def quant_fwd_nvfp4(x, p: int = 2, tensor_scale=None, out=None, stream=None):
     _check(lib().mxnorm_quant_fwd_nvfp4(x.data_ptr(), T, H, int(p), g, codes.data_ptr(), scales.data_ptr(),
                                         inv.data_ptr(), _stream_ptr(x.device, stream)))
     return codes, scales, inv
+
+
+SCALE_LAYOUT = {"row_major": 0, "mma": 1}
+
+
+def mma_scale_bytes(rows: int, H: int) -> int:
+    """Bytes of an MMA-layout scale buffer for rows x H (H % 128 == 0)."""
+    n = lib().mxnorm_mma_scale_bytes(rows, H)
+    if n < 0:
+        raise ValueError("the MMA scale layout needs H % 128 == 0")
+    return n
+
+
+def _scale_buffer(rows, H, layout, device):
+    import torch
+    if layout == "mma":
+        return torch.empty((mma_scale_bytes(rows, H),), dtype=torch.uint8, device=device)
+    return torch.empty((rows, H // 32), dtype=torch.uint8, device=device)
+
+
+def quant_fwd_mma(x, p: int = 2, fmt: str = "mxfp8", stream=None):
+    """mxnorm_quant_fwd with the scales in the tensor-core MMA atom layout
+    (for mxnorm_linear_fwd).  Returns (codes, scales (flat uint8), inv_rms)."""
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous bfloat16 CUDA tensor")
+    H = x.shape[-1]
+    T = x.numel() // H if H else 0
+    codes = torch.empty(tuple(x.shape[:-1]) + (code_bytes(H, fmt),), dtype=torch.uint8, device=x.device)
+    scales = _scale_buffer(T, H, "mma", x.device)
+    inv = torch.empty(tuple(x.shape[:-1]), dtype=torch.float32, device=x.device)
+    _check(lib().mxnorm_quant_fwd_layout(x.data_ptr(), T, H, int(p), FMT[fmt], codes.data_ptr(), scales.data_ptr(),
+                                         inv.data_ptr(), 1, _stream_ptr(x.device, stream)))
+    return codes, scales, inv
+
+
+def mx_cast(x, layout: str = "row_major", stream=None):
+    """MXFP8 E4M3 cast alone (no estimator) of bf16 rows: (codes, scales)."""
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous bfloat16 CUDA tensor")
+    H = x.shape[-1]
+    T = x.numel() // H if H else 0
+    codes = torch.empty(tuple(x.shape), dtype=torch.uint8, device=x.device)
+    scales = _scale_buffer(T, H, layout, x.device)
+    _check(lib().mx_cast_fwd(x.data_ptr(), T, H, 0, codes.data_ptr(), scales.data_ptr(), SCALE_LAYOUT[layout],
+                             _stream_ptr(x.device, stream)))
+    return codes, scales
+
+
+def linear_fwd(x_codes, x_scales, inv_rms, w_codes, w_scales, out=None, stream=None):
+    """MXNormLinear's consumer GEMM on the tensor cores: out = bf16(inv_rms[t]
+    * sum_k x^[t,k] w^[n,k]); scales in the MMA layout.  Returns out [T, N]."""
+    import torch
+    T, K = x_codes.shape
+    N = w_codes.shape[0]
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=x_codes.device)
+    _check(lib().mxnorm_linear_fwd(x_codes.data_ptr(), x_scales.data_ptr(), inv_rms.data_ptr(), w_codes.data_ptr(),
+                                   w_scales.data_ptr(), T, K, N, out.data_ptr(), _stream_ptr(x_codes.device, stream)))
+    return out
 
 
 def bwd_ste(x, dy, inv_rms, out=None, stream=None):

@@ -105,6 +105,71 @@ int mxnorm_quant_fwd_ex(const void* x, int64_t T, int64_t H, int p, int fmt, voi
   return MXNORM_OK;
 }
 
+int64_t mxnorm_mma_scale_bytes(int64_t rows, int64_t H) {
+  if (rows < 0 || H <= 0 || H % 128 != 0) return -1;
+  return ((rows + 127) / 128) * (H / 128) * 512;
+}
+
+int mxnorm_quant_fwd_layout(const void* x, int64_t T, int64_t H, int p, int fmt, void* codes, uint8_t* scales,
+                            float* inv_rms, int scale_layout, void* stream) {
+  if (scale_layout == MXNORM_SCALE_ROW_MAJOR)
+    return mxnorm_quant_fwd_ex(x, T, H, p, fmt, codes, scales, inv_rms, MXNORM_VARIANT_AUTO, stream);
+  g_last_error.clear();
+  if (scale_layout != MXNORM_SCALE_MMA) return fail(MXNORM_ERR_INVALID_ARG, "unknown scale_layout %d", scale_layout);
+  if (p != 1 && p != 2) return fail(MXNORM_ERR_INVALID_ARG, "p = %d is not 1 or 2", p);
+  if (fmt < 0 || fmt >= kNumFmts) return fail(MXNORM_ERR_INVALID_ARG, "unknown fmt %d", fmt);
+  int st = check_common(x, T, H, codes, scales, inv_rms);
+  if (st != MXNORM_OK || T == 0) return st;
+  if (H % 128 != 0) return fail(MXNORM_ERR_INVALID_ARG, "the MMA scale layout needs H %% 128 == 0 (H = %lld)", (long long)H);
+  WarpRowArgs a{x, T, H, p, fmt, codes, scales, inv_rms};
+  a.scale_tiled = 1;
+  cudaError_t err = launch_mxnorm_warp_row(a, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "mxnorm_quant_fwd_layout launch");
+  return MXNORM_OK;
+}
+
+int mx_cast_fwd(const void* x, int64_t T, int64_t H, int fmt, void* codes, uint8_t* scales, int scale_layout,
+                void* stream) {
+  g_last_error.clear();
+  if (fmt != MXNORM_FMT_MXFP8_E4M3) return fail(MXNORM_ERR_UNSUPPORTED, "mx_cast_fwd supports MXFP8 E4M3 only");
+  if (scale_layout != MXNORM_SCALE_ROW_MAJOR && scale_layout != MXNORM_SCALE_MMA)
+    return fail(MXNORM_ERR_INVALID_ARG, "unknown scale_layout %d", scale_layout);
+  if (T < 0) return fail(MXNORM_ERR_INVALID_ARG, "T = %lld < 0", (long long)T);
+  if (H <= 0 || H % kBlock != 0)
+    return fail(MXNORM_ERR_INVALID_ARG, "H = %lld is not a positive multiple of 32", (long long)H);
+  if (H > MXNORM_MAX_H)
+    return fail(MXNORM_ERR_UNSUPPORTED, "H = %lld exceeds MXNORM_MAX_H = %d", (long long)H, MXNORM_MAX_H);
+  if (scale_layout == MXNORM_SCALE_MMA && H % 128 != 0)
+    return fail(MXNORM_ERR_INVALID_ARG, "the MMA scale layout needs H %% 128 == 0 (H = %lld)", (long long)H);
+  if (T == 0) return MXNORM_OK;
+  if (!x || !codes || !scales) return fail(MXNORM_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(x, 16) || !aligned(codes, 16)) return fail(MXNORM_ERR_MISALIGNED, "x and codes need 16-byte alignment");
+  WarpRowArgs a{x, T, H, 2, fmt, codes, scales, nullptr};
+  a.scale_tiled = scale_layout == MXNORM_SCALE_MMA;
+  cudaError_t err = launch_mx_cast_warp_row(a, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "mx_cast_fwd launch");
+  return MXNORM_OK;
+}
+
+int mxnorm_linear_fwd(const void* x_codes, const uint8_t* x_scales, const float* inv_rms, const void* w_codes,
+                      const uint8_t* w_scales, int64_t T, int64_t K, int64_t N, void* out, void* stream) {
+  g_last_error.clear();
+  if (T < 0) return fail(MXNORM_ERR_INVALID_ARG, "T = %lld < 0", (long long)T);
+  if (K <= 0 || K % 128 != 0) return fail(MXNORM_ERR_INVALID_ARG, "K = %lld is not a positive multiple of 128", (long long)K);
+  if (N <= 0 || N % 256 != 0) return fail(MXNORM_ERR_INVALID_ARG, "N = %lld is not a positive multiple of 256", (long long)N);
+  if (K > MXNORM_MAX_H || N > (1 << 24)) return fail(MXNORM_ERR_UNSUPPORTED, "K or N too large");
+  if (T == 0) return MXNORM_OK;
+  if (!x_codes || !x_scales || !inv_rms || !w_codes || !w_scales || !out)
+    return fail(MXNORM_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(x_codes, 16) || !aligned(w_codes, 16) || !aligned(x_scales, 16) || !aligned(w_scales, 16) ||
+      !aligned(out, 16) || !aligned(inv_rms, 4))
+    return fail(MXNORM_ERR_MISALIGNED, "codes, scales and out need 16-byte alignment, inv_rms 4-byte");
+  cudaError_t err = launch_mxfp8_linear(LinearArgs{x_codes, x_scales, inv_rms, w_codes, w_scales, T, K, N, out},
+                                        static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "mxnorm_linear_fwd launch (tensor maps or launch)");
+  return MXNORM_OK;
+}
+
 int mxnorm_quant_fwd(const void* x, int64_t T, int64_t H, int p, int fmt, void* codes,
                      uint8_t* scales, float* inv_rms, void* stream) {
   return mxnorm_quant_fwd_ex(x, T, H, p, fmt, codes, scales, inv_rms, MXNORM_VARIANT_AUTO, stream);
@@ -192,8 +257,11 @@ int mxnorm_abi_version(void) { return MXNORM_ABI_VERSION; }
 
 int mxnorm_device_errors(uint32_t* flags, int clear) {
   if (!flags) return fail(MXNORM_ERR_INVALID_ARG, "NULL flags");
-  cudaError_t err = read_device_error_word(flags, clear != 0);
-  if (err != cudaSuccess) return cuda_fail(err, "reading the device error word");
+  uint32_t tiled = 0, linear = 0;
+  cudaError_t err = read_device_error_word(&tiled, clear != 0);
+  if (err == cudaSuccess) err = read_linear_error_word(&linear, clear != 0);
+  if (err != cudaSuccess) return cuda_fail(err, "reading the device error words");
+  *flags = (tiled & 1u) | ((linear & 1u) << 1);
   return MXNORM_OK;
 }
 

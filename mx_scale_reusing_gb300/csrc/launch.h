@@ -16,6 +16,7 @@ struct WarpRowArgs {
   void* codes;        // u8 [T, H] (E4M3) or [T, H/2] (E2M1)
   uint8_t* scales;    // u8 [T, H/32]
   float* inv_rms;     // f32 [T] (unused by the cast-only form)
+  int scale_tiled = 0;  // 1: scales in the MMA atom layout (see scale_ptr in mx_row.cuh)
 };
 
 struct RmsNormArgs {
@@ -47,6 +48,18 @@ struct Nvfp4Args {
   float* inv_rms;      // f32 [T]
 };
 
+struct LinearArgs {
+  const void* x_codes;       // E4M3 [T, K]
+  const uint8_t* x_scales;   // E8M0, MMA atom layout, ceil(T/128) x K/128 atoms
+  const float* inv_rms;      // f32 [T]
+  const void* w_codes;       // E4M3 [N, K]
+  const uint8_t* w_scales;   // E8M0, MMA atom layout, N/128 x K/128 atoms
+  int64_t T;
+  int64_t K;
+  int64_t N;
+  void* out;                 // bf16 [T, N]
+};
+
 struct TiledArgs {
   WarpRowArgs base;
   unsigned int* error_flag;  // device word set when a bounded wait gives up
@@ -64,6 +77,8 @@ cudaError_t launch_mxnorm_tiled(const TiledArgs& a, cudaStream_t s);
 bool tiled_supported(int64_t H, int fmt);
 cudaError_t launch_mxnorm_bwd_ste(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_nvfp4(const Nvfp4Args& a, cudaStream_t s);
+cudaError_t launch_mxfp8_linear(const LinearArgs& a, cudaStream_t s);
+cudaError_t read_linear_error_word(uint32_t* out, bool clear);
 cudaError_t launch_absmax_bf16(const void* x, int64_t n, float* amax, cudaStream_t s);
 
 // Replace the calling thread's message returned by mxnorm_last_error().

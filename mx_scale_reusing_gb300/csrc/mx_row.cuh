@@ -148,6 +148,19 @@ __device__ __forceinline__ int cast_lane(const uint32_t (&w)[VEC / 2], bool vali
   return nonfinite ? kExpNone : e;
 }
 
+// Address of the E8M0 byte of (row, block kb) for a row of K blocks.
+// Row-major: scales[row * K + kb].  MMA-tiled (tiled != 0, K % 4 == 0): the
+// 512-byte atoms the block-scaled tensor-core MMA reads, one per 128 rows x
+// 4 blocks, atoms ordered row-tile-major; inside an atom the byte of
+// (r, k) sits at (r % 32) * 16 + (r / 32 % 4) * 4 + k % 4, so one
+// tcgen05.cp of 32 lanes x 16 bytes lands row r's 4 scales in TMEM lane
+// r % 32, column r / 32.
+__device__ __forceinline__ uint8_t* scale_ptr(uint8_t* scales, int64_t row, int kb, int K, int tiled) {
+  if (!tiled) return scales + row * (int64_t)K + kb;
+  const int64_t atom = (row >> 7) * (int64_t)(K >> 2) + (kb >> 2);
+  return scales + atom * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (kb & 3);
+}
+
 // Power mean of a row from the exponents each lane collected (ev[c] for its
 // chunks, meaningful where own[c]): m = the row's largest exponent (warp
 // max), then the fixed-point sum sum_k 2^(F + p (e_k - m)) (terms below 2^0
@@ -189,7 +202,7 @@ template <int FMT, int VEC, int NCHUNK, int AHEAD, bool EXACT, bool LOAD32, bool
 __device__ __forceinline__ void mx_rows_stream(const uint16_t* __restrict__ x, int64_t T, int H,
                                                uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                                float* __restrict__ inv_rms, int p, int64_t row,
-                                               int64_t rstride) {
+                                               int64_t rstride, int scale_tiled) {
   static_assert(NCHUNK % AHEAD == 0, "the ring must tile the row");
   using Tr = FmtTraits<FMT>;
   constexpr int LPB = kBlock / VEC;
@@ -217,7 +230,6 @@ __device__ __forceinline__ void mx_rows_stream(const uint16_t* __restrict__ x, i
   for (; row < T; row += rstride) {
     const int64_t next = row + rstride;
     uint8_t* cr = codes + row * code_row;
-    uint8_t* sr = scales + row * (int64_t)K;
     int ev[NCHUNK];
     bool own[NCHUNK];
 #pragma unroll
@@ -230,7 +242,8 @@ __device__ __forceinline__ void mx_rows_stream(const uint16_t* __restrict__ x, i
       else if (next < T) issue(next, cc - NCHUNK, buf[c % AHEAD]);
       const int e0 = c * CE + lane * VEC;
       const bool valid = EXACT || e0 < Hc;
-      ev[c] = cast_lane<FMT, VEC>(w, valid, cr + (Tr::fp4 ? e0 / 2 : e0), sr + e0 / kBlock, lead);
+      ev[c] = cast_lane<FMT, VEC>(w, valid, cr + (Tr::fp4 ? e0 / 2 : e0),
+                                  scale_ptr(scales, row, e0 / kBlock, K, scale_tiled), lead);
       own[c] = valid && lead;
     }
     if constexpr (ESTIMATE) {
@@ -245,8 +258,8 @@ __device__ __forceinline__ void mx_rows_stream(const uint16_t* __restrict__ x, i
 // 0 handles any H in batches of four chunks with the running-maximum
 // power-mean accumulator.  Every lane of the warp must call it.
 template <int FMT, int VEC, int NCHUNK, bool ESTIMATE, class Load>
-__device__ __forceinline__ void mx_row(Load load, int H, int p, uint8_t* cr, uint8_t* sr,
-                                       float* inv_dst) {
+__device__ __forceinline__ void mx_row(Load load, int H, int p, uint8_t* cr, uint8_t* scales, int64_t row,
+                                       int scale_tiled, float* inv_dst) {
   using Tr = FmtTraits<FMT>;
   constexpr int LPB = kBlock / VEC;
   constexpr int CE = 32 * VEC;
@@ -272,7 +285,8 @@ __device__ __forceinline__ void mx_row(Load load, int H, int p, uint8_t* cr, uin
     for (int c = 0; c < NCHUNK; ++c) {
       const int e0 = c * CE + lane * VEC;
       const bool valid = e0 < H;
-      ev[c] = cast_lane<FMT, VEC>(w[c], valid, cr + (Tr::fp4 ? e0 / 2 : e0), sr + e0 / kBlock, lead);
+      ev[c] = cast_lane<FMT, VEC>(w[c], valid, cr + (Tr::fp4 ? e0 / 2 : e0),
+                                  scale_ptr(scales, row, e0 / kBlock, K, scale_tiled), lead);
       own[c] = valid && lead;
     }
     if constexpr (ESTIMATE) {
@@ -301,7 +315,8 @@ __device__ __forceinline__ void mx_row(Load load, int H, int p, uint8_t* cr, uin
         if (c0 + b < nchunk) {
           const int e0 = (c0 + b) * CE + lane * VEC;
           const bool valid = e0 < H;
-          const int e = cast_lane<FMT, VEC>(w[b], valid, cr + (Tr::fp4 ? e0 / 2 : e0), sr + e0 / kBlock, lead);
+          const int e = cast_lane<FMT, VEC>(w[b], valid, cr + (Tr::fp4 ? e0 / 2 : e0),
+                                            scale_ptr(scales, row, e0 / kBlock, K, scale_tiled), lead);
           if (ESTIMATE && valid && lead) {
             if (e == kExpNone) row_nonfinite = true;
             else pm_add(acc, e, p);

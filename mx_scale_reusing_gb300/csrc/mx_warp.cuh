@@ -28,11 +28,11 @@ constexpr int kWarpsPerCta = 8;
 template <int FMT, int VEC, int NCHUNK, int AHEAD, bool EXACT, bool LOAD32, bool ESTIMATE, int MINB>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, MINB)
     mx_warp_row_kernel(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
-                       uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p) {
+                       uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p, int scale_tiled) {
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
   mx_rows_stream<FMT, VEC, NCHUNK, AHEAD, EXACT, LOAD32, ESTIMATE>(x, T, H, codes, scales, inv_rms, p,
-                                                                   warp0, nwarps);
+                                                                   warp0, nwarps, scale_tiled);
 }
 
 // Any H (a multiple of 32): batches of four chunks per row.
@@ -40,7 +40,7 @@ template <int FMT, int VEC, bool LOAD32, bool ESTIMATE>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     mx_warp_row_generic_kernel(const uint16_t* __restrict__ x, int64_t T, int H,
                                uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                               float* __restrict__ inv_rms, int p) {
+                               float* __restrict__ inv_rms, int p, int scale_tiled) {
   using Tr = FmtTraits<FMT>;
   const int K = H / kBlock;
   const int64_t code_row = Tr::fp4 ? (int64_t)(H / 2) : (int64_t)H;
@@ -49,8 +49,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   for (int64_t row = warp0; row < T; row += nwarps) {
     const uint16_t* xr = x + row * (int64_t)H;
     auto load = [xr](int e0, uint32_t (&w)[VEC / 2]) { load_lane<VEC, LOAD32>(xr + e0, w); };
-    mx_row<FMT, VEC, 0, ESTIMATE>(load, H, p, codes + row * code_row, scales + row * (int64_t)K,
-                                  inv_rms + row);
+    mx_row<FMT, VEC, 0, ESTIMATE>(load, H, p, codes + row * code_row, scales, row, scale_tiled, inv_rms + row);
   }
 }
 
@@ -59,7 +58,8 @@ cudaError_t launch_kernel(Kern kern, const WarpRowArgs& a, cudaStream_t stream) 
   const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kWarpsPerCta * 32,
                                    (a.T + kWarpsPerCta - 1) / kWarpsPerCta);
   kern<<<grid, kWarpsPerCta * 32, 0, stream>>>(static_cast<const uint16_t*>(a.x), a.T, (int)a.H,
-                                               static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms, a.p);
+                                               static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms, a.p,
+                                               a.scale_tiled);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,335 @@
+// mxnorm_linear.cu -- consumer side of MXNormLinear on the 5th-generation
+// tensor cores: an MXFP8 block-scaled GEMM whose epilogue applies MXNorm's
+// per-row inverse RMS.
+//
+// "MXNorm: Reusing MXFP block scales for efficient tensor normalisation",
+// Resumen tecnico, 2. Metodologia, "Implementacion": MXNormLinear folds the
+// norm's gain into the next linear layer's weight, so the layer computes
+//     out[t, n] = rho~[t] * sum_k x^[t, k] w'^[n, k]
+// with x^ the MXFP8 codes and E8M0 block scales of the row (mxnorm_quant_fwd
+// with the MMA scale layout), rho~ = inv_rms, and w'^ the MXFP8 cast of
+// W' = diag(c gamma) W, i.e. one row per output feature, quantised along K
+// (mx_cast_fwd).  The row scale commutes with the matmul, so it is applied
+// once per output element in the epilogue.
+//
+// Tiling: 128 x 256 output tiles (one tcgen05.mma M = 128, N = 256 per
+// 32-element K step, cta_group::1, kind::mxf8f6f4 with 1X E8M0 block
+// scales), K staged 128 bytes at a time through a 4-deep shared-memory ring.
+// Persistent CTAs, one per SM, warp-specialised:
+//   warp 0 lane 0  TMA producer: 2-D tiled loads of the x and w code tiles
+//                  (128-byte swizzle) plus 1-D bulk copies of the 512-byte
+//                  scale atoms, completing on the stage's "full" mbarrier;
+//   warp 1 lane 0  MMA issuer: per stage, tcgen05.cp of the scale atoms
+//                  into TMEM (32 lanes x 128 bits, replicated to the 4 lane
+//                  quadrants), four tcgen05.mma, then tcgen05.commit to the
+//                  stage's "empty" mbarrier; after a tile's last stage a
+//                  commit to "acc_full";
+//   warps 2-5      epilogue: tcgen05.ld of the fp32 accumulators (each warp
+//                  its TMEM lane quadrant = 32 rows), times rho~[row],
+//                  rounded to bf16, stored; then "acc_empty" frees TMEM for
+//                  the next tile.
+// TMEM: accumulators in columns 0-255, the scale factors of ring stage s in
+// columns 256 + 16 s (A: 4 columns, B: 8).  Every mbarrier wait is bounded
+// (2 s by %globaltimer); on expiry the waiter sets bit 1 of the device error
+// word and the kernel winds down, waiting (bounded) for its own bulk copies
+// and MMAs before it frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "launch.h"
+#include "mx_device.cuh"
+
+namespace mxnorm {
+
+__device__ unsigned int g_linear_error_word = 0u;
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128;     // BK in bytes = E4M3 elements
+constexpr int kStages = 4;
+constexpr int kStageA = BM * BK;                 // 16 KiB
+constexpr int kStageB = BN * BK;                 // 32 KiB
+constexpr int kStageSF = 512 + 2 * 512;          // one A scale atom, two B scale atoms
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTxBytes = kStageA + kStageB + kStageSF;
+constexpr unsigned long long kWaitNs = 2000000000ull;
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * (kStageA + kStageB + kStageSF) + 256;
+
+__device__ __forceinline__ uint32_t saddr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+// Bounded wait; false (and bit 1 of the error word) on timeout.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
+  if (try_wait(bar, parity)) return true;
+  const unsigned long long t0 = gtimer();
+  while (!try_wait(bar, parity)) {
+    if (gtimer() - t0 > kWaitNs) {
+      atomicOr(&g_linear_error_word, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
+// K-major operand tile with 128-byte swizzle: 8-row atoms of 1024 bytes,
+// leading offset unused, stride 1024 bytes, descriptor version 1.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// A 512-byte scale atom as a plain 32-row x 16-byte matrix (8-row groups
+// 128 bytes apart) for tcgen05.cp.
+__device__ __forceinline__ uint64_t desc_atom(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: E4M3 x E4M3,
+// both K-major, E8M0 scales, M = 128, N = 256, scale byte `sf` of each
+// 32-bit TMEM scale word for A and B (the 32-element K step within the
+// 128-element stage).
+__device__ __forceinline__ uint32_t idesc_mxf8(int sf) {
+  return ((uint32_t)sf << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24) |
+         ((uint32_t)sf << 29);
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_512(uint32_t dst, const void* src, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 512, [%2];" ::"r"(dst),
+               "l"(src), "r"(bar)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mxfp8_linear_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                        const uint8_t* __restrict__ sf_x, const uint8_t* __restrict__ sf_w,
+                        const float* __restrict__ inv_rms, uint16_t* __restrict__ out, int64_t T, int K, int N) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + kStages * kStageA;
+  uint8_t* sSF = sB + kStages * kStageB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSF + kStages * kStageSF);
+  // bars: full[kStages], empty[kStages], acc_full, acc_empty, drain; then the TMEM base word
+  const uint32_t full0 = saddr(bars), empty0 = saddr(bars + kStages);
+  const uint32_t acc_full = saddr(bars + 2 * kStages), acc_empty = saddr(bars + 2 * kStages + 1);
+  const uint32_t drain = saddr(bars + 2 * kStages + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 3);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_n = N / BN, num_kt = K / BK;
+  const int64_t num_m = (T + BM - 1) / BM;
+  const int64_t tiles = num_m * num_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(full0 + 8 * s));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * s));
+    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(acc_full));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(acc_empty));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(drain));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int64_t it = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        const int64_t mt = tile / num_n;
+        const int nt = (int)(tile % num_n);
+        for (int kt = 0; kt < num_kt; ++kt, ++it) {
+          const int s = (int)(it % kStages);
+          const uint32_t use = (uint32_t)(it / kStages);
+          if (use > 0 && !(ok = wait_bounded(empty0 + 8 * s, (use - 1) & 1u))) break;
+          const uint32_t fb = full0 + 8 * s;
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(kTxBytes) : "memory");
+          tma_2d(saddr(sA + s * kStageA), &tm_x, kt * BK, (int)(mt * BM), fb);
+          tma_2d(saddr(sB + s * kStageB), &tm_w, kt * BK, nt * BN, fb);
+          uint8_t* sf = sSF + s * kStageSF;
+          bulk_512(saddr(sf), sf_x + (mt * num_kt + kt) * 512, fb);
+          bulk_512(saddr(sf + 512), sf_w + ((int64_t)(2 * nt) * num_kt + kt) * 512, fb);
+          bulk_512(saddr(sf + 1024), sf_w + ((int64_t)(2 * nt + 1) * num_kt + kt) * 512, fb);
+        }
+      }
+      // every copy issued must have landed before the CTA may exit
+      for (int64_t i = (it > kStages ? it - kStages : 0); i < it; ++i)
+        (void)wait_bounded(full0 + 8 * (int)(i % kStages), (uint32_t)(i / kStages) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int64_t it = 0, tcount = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++tcount) {
+        if (tcount > 0 && !(ok = wait_bounded(acc_empty, (uint32_t)((tcount - 1) & 1)))) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        for (int kt = 0; kt < num_kt; ++kt, ++it) {
+          const int s = (int)(it % kStages);
+          if (!(ok = wait_bounded(full0 + 8 * s, (uint32_t)(it / kStages) & 1u))) break;
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t tsf = tmem + 256 + 16 * s;
+          const uint32_t sf = saddr(sSF + s * kStageSF);
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsf), "l"(desc_atom(sf)));
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 4), "l"(desc_atom(sf + 512)));
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 8), "l"(desc_atom(sf + 1024)));
+          const uint32_t a0 = saddr(sA + s * kStageA), b0 = saddr(sB + s * kStageB);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t accum = (kt | j) ? 1u : 0u;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                    tmem),
+                "l"(desc_sw128(a0 + 32 * j)), "l"(desc_sw128(b0 + 32 * j)), "r"(idesc_mxf8(j)), "r"(tsf), "r"(tsf + 4),
+                "r"(accum));
+          }
+          asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty0 + 8 * s)
+                       : "memory");
+        }
+        if (!ok) break;
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(acc_full)
+                     : "memory");
+      }
+      // all MMAs and scale copies of this thread complete before TMEM is freed
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(drain) : "memory");
+      (void)wait_bounded(drain, 0);
+    }
+  } else {
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int64_t rin = 32 * quad + lane;
+    int64_t tcount = 0;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tcount) {
+      if (!wait_bounded(acc_full, (uint32_t)(tcount & 1))) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int64_t row = (tile / num_n) * BM + rin;
+      const int n0 = (int)(tile % num_n) * BN;
+      const bool valid = row < T;
+      const float r = valid ? inv_rms[row] : 0.0f;
+      uint16_t* orow = out + row * (int64_t)N + n0;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+            "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+              "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+              "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+              "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+            : "r"(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)c0));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (valid) {
+          uint32_t o[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), r),
+                                                           __fmul_rn(__uint_as_float(v[2 * i + 1]), r));
+            o[i] = *reinterpret_cast<const uint32_t*>(&b);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) stg16(orow + c0 + 8 * q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acc_empty) : "memory");
+    }
+  }
+
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// rows x K uint8 codes, box of `box_rows` rows x 128 bytes, 128-byte swizzle
+bool encode_codes(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_mxfp8_linear(const LinearArgs& a, cudaStream_t s) {
+  CUtensorMap tm_x, tm_w;
+  if (!encode_codes(&tm_x, a.x_codes, a.T, a.K, BM) || !encode_codes(&tm_w, a.w_codes, a.N, a.K, BN))
+    return cudaErrorInvalidValue;
+  const void* kern = reinterpret_cast<const void*>(mxfp8_linear_kernel);
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const int64_t tiles = ((a.T + BM - 1) / BM) * (a.N / BN);
+  const int grid = persistent_grid(kern, kThreads, tiles, kSmemBytes);
+  mxfp8_linear_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, a.x_scales, a.w_scales, a.inv_rms,
+                                                         static_cast<uint16_t*>(a.out), a.T, (int)a.K, (int)a.N);
+  return cudaGetLastError();
+}
+
+cudaError_t read_linear_error_word(uint32_t* out, bool clear) {
+  unsigned int v = 0;
+  cudaError_t err = cudaMemcpyFromSymbol(&v, g_linear_error_word, sizeof v);
+  if (err != cudaSuccess) return err;
+  *out = v;
+  if (clear) {
+    const unsigned int zero = 0;
+    err = cudaMemcpyToSymbol(g_linear_error_word, &zero, sizeof zero);
+  }
+  return err;
+}
+
+}  // namespace mxnorm

@@ -171,8 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t srow = ring0 + (uint32_t)(s * stage_bytes + r * row_bytes);
       auto load = [srow](int e0, uint32_t (&w)[VEC / 2]) { lds_lane<VEC>(srow + 2u * (uint32_t)e0, w); };
       const int64_t code_row = Tr::fp4 ? (int64_t)(H / 2) : (int64_t)H;
-      mx_row<FMT, VEC, NCHUNK, true>(load, H, p, codes + row * code_row, scales + row * (int64_t)(H / kBlock),
-                                     inv_rms + row);
+      mx_row<FMT, VEC, NCHUNK, true>(load, H, p, codes + row * code_row, scales, row, 0, inv_rms + row);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);

@@ -99,6 +99,22 @@ def test_nvfp4_validation(L):
     assert L.mxnorm_absmax_bf16(FAKE, 8, None, None) == 1
 
 
+def test_linear_and_layout_validation(L):
+    assert L.mxnorm_mma_scale_bytes(300, 768) == 3 * 6 * 512
+    assert L.mxnorm_mma_scale_bytes(300, 96) == -1
+    lin = L.mxnorm_linear_fwd
+    assert lin(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 128, 256, FAKE, None) == 0
+    assert lin(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 96, 256, FAKE, None) == 1
+    assert lin(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 128, 128, FAKE, None) == 1
+    assert lin(FAKE, FAKE, FAKE, None, FAKE, 8, 128, 256, FAKE, None) == 1
+    assert lin(FAKE, FAKE + 8, FAKE, FAKE, FAKE, 8, 128, 256, FAKE, None) == 3
+    q = L.mxnorm_quant_fwd_layout
+    assert q(FAKE, 8, 96, 2, 0, FAKE, FAKE, FAKE, 1, None) == 1
+    assert q(FAKE, 8, 128, 2, 0, FAKE, FAKE, FAKE, 7, None) == 1
+    assert L.mx_cast_fwd(FAKE, 8, 128, 1, FAKE, FAKE, 0, None) == 2
+    assert L.mx_cast_fwd(FAKE, 8, 96, 0, FAKE, FAKE, 1, None) == 1
+
+
 def test_python_binding_raises_on_status(L):
     with pytest.raises(mx.MXNormError) as ei:
         mx.mxnorm_quant_fwd(FAKE, 8, 48, 2, 0, FAKE, FAKE, FAKE)
