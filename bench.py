@@ -279,6 +279,47 @@ def run_gpu(args):
                                 "bytes_per_row": 2 * H + H // 2 + H // 16 + 4}
     del c4n, s4n
 
+    # MXNormLinear on the tensor cores: the same rows quantised with the
+    # scales in the MMA atom layout, then the block-scaled GEMM against a
+    # 4096 x 4096 MXFP8 weight (a Llama-3-8B projection) with the inv_rms
+    # epilogue.  FLOP/s against the fp8 peak = measured bf16 x 2 (nominal ratio).
+    Nw = 4096
+    gw = torch.Generator(device=dev).manual_seed(7)
+    wt = (torch.randn((Nw, H), device=dev, generator=gw) * 0.02).to(torch.bfloat16)
+    w_codes, w_scales = mx.mx_cast(wt, "mma")
+    del wt
+    xq_codes = torch.empty((T, H), dtype=torch.uint8, device=dev)
+    xq_scales = torch.empty((mx.mma_scale_bytes(T, H),), dtype=torch.uint8, device=dev)
+    xq_inv = torch.empty((T,), dtype=torch.float32, device=dev)
+    lin_out = torch.empty((T, Nw), dtype=torch.bfloat16, device=dev)
+
+    def quant_mma_step(i):
+        st = mx.lib().mxnorm_quant_fwd_layout(xs[i].data_ptr(), T, H, 2, 0, xq_codes.data_ptr(), xq_scales.data_ptr(),
+                                              xq_inv.data_ptr(), 1, ctypes.c_void_p(sptr))
+        if st:
+            raise RuntimeError(mx.lib().mxnorm_last_error().decode())
+
+    def linear_step(i):
+        st = mx.lib().mxnorm_linear_fwd(xq_codes.data_ptr(), xq_scales.data_ptr(), xq_inv.data_ptr(),
+                                        w_codes.data_ptr(), w_scales.data_ptr(), T, H, Nw, lin_out.data_ptr(),
+                                        ctypes.c_void_p(sptr))
+        if st:
+            raise RuntimeError(mx.lib().mxnorm_last_error().decode())
+
+    perq, _ = time_launches(torch, stream, quant_mma_step, sec_steps, 5, nbuf)
+    lin_steps = max(10, sec_steps // 10)
+    perl, _ = time_launches(torch, stream, linear_step, lin_steps, 3, nbuf)
+    mq, ml = statistics.fmean(perq), statistics.fmean(perl)
+    fp8_peak = 2.0 * float(peaks.get("bf16_tflops", 1900.0))
+    tflops = 2.0 * T * H * Nw / (ml * 1e-3) / 1e12
+    extra["mxnorm_quant_mma_layout_p2"] = {"ms": round(mq, 5), "GB/s": gbs(abytes, mq),
+                                           "frac": round(gbs(abytes, mq) / hbm_peak, 4)}
+    extra["mxnorm_linear_fwd_65536x4096x4096"] = {
+        "ms": round(ml, 5), "TFLOP/s": round(tflops, 1), "frac_of_fp8_peak": round(tflops / fp8_peak, 4),
+        "fp8_peak_TFLOPs": round(fp8_peak, 1), "peak_source": f"{peak_kind} bf16_tflops x 2 (fp8/bf16 nominal)",
+        "layer_tokens_per_s": round(T / ((mq + ml) * 1e-3), 1)}
+    del w_codes, w_scales, xq_codes, xq_scales, xq_inv, lin_out
+
     y_ws = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
 
     def base_step(i):

@@ -26,8 +26,8 @@
 //                  commit to "acc_full";
 //   warps 2-5      epilogue: tcgen05.ld of the fp32 accumulators (each warp
 //                  its TMEM lane quadrant = 32 rows), times rho~[row],
-//                  rounded to bf16, stored; then "acc_empty" frees TMEM for
-//                  the next tile.
+//                  rounded to packed bf16 in registers; "acc_empty" then
+//                  frees TMEM for the next tile's MMAs before the stores.
 // TMEM: accumulators in columns 0-255, the scale factors of ring stage s in
 // columns 256 + 16 s (A: 4 columns, B: 8).  Every mbarrier wait is bounded
 // (2 s by %globaltimer); on expiry the waiter sets bit 1 of the device error
@@ -239,8 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = (int)(tile % num_n) * BN;
       const bool valid = row < T;
       const float r = valid ? inv_rms[row] : 0.0f;
-      uint16_t* orow = out + row * (int64_t)N + n0;
-#pragma unroll 1
+      // Pull the whole 128 x 256 tile out of TMEM first (as packed bf16),
+      // hand TMEM back to the MMA issuer, then store: the next tile's MMAs
+      // run while these stores drain.
+      uint32_t o[BN / 2];
+#pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t v[32];
         asm volatile(
@@ -252,21 +255,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
             : "r"(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)c0));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (valid) {
-          uint32_t o[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), r),
-                                                           __fmul_rn(__uint_as_float(v[2 * i + 1]), r));
-            o[i] = *reinterpret_cast<const uint32_t*>(&b);
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) stg16(orow + c0 + 8 * q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        for (int i = 0; i < 16; ++i) {
+          const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), r),
+                                                         __fmul_rn(__uint_as_float(v[2 * i + 1]), r));
+          o[c0 / 2 + i] = *reinterpret_cast<const uint32_t*>(&b);
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acc_empty) : "memory");
+      if (valid) {
+        uint16_t* orow = out + row * (int64_t)N + n0;
+#pragma unroll
+        for (int q = 0; q < BN / 8; ++q) stg16(orow + 8 * q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      }
     }
   }
 
