@@ -27,7 +27,9 @@
 //   warps 2-5      epilogue: tcgen05.ld of the fp32 accumulators (each warp
 //                  its TMEM lane quadrant = 32 rows), times rho~[row],
 //                  rounded to packed bf16 in registers; "acc_empty" then
-//                  frees TMEM for the next tile's MMAs before the stores.
+//                  frees TMEM for the next tile's MMAs, and the rows leave
+//                  through per-warp 4 KiB swizzled staging buffers as TMA
+//                  tensor stores of 32 x 64 bf16 boxes.
 // TMEM: accumulators in columns 0-255, the scale factors of ring stage s in
 // columns 256 + 16 s (A: 4 columns, B: 8).  Every mbarrier wait is bounded
 // (2 s by %globaltimer); on expiry the waiter sets bit 1 of the device error
@@ -56,7 +58,10 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTxBytes = kStageA + kStageB + kStageSF;
 constexpr unsigned long long kWaitNs = 2000000000ull;
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * (kStageA + kStageB + kStageSF) + 256;
+constexpr int kOutChunk = 64;                    // bf16 columns per TMA store box (128 bytes)
+constexpr int kOutStage = 32 * kOutChunk * 2;    // one epilogue warp's 32-row staging buffer, 4 KiB
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * (kStageA + kStageB + kStageSF) +
+                              4 * kOutStage + 256;
 
 __device__ __forceinline__ uint32_t saddr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -124,16 +129,37 @@ __device__ __forceinline__ void bulk_512(uint32_t dst, const void* src, uint32_t
                : "memory");
 }
 
+// Persistent tile order: groups of kGroupM row tiles walk the column tiles
+// together (row tile fastest inside a group), so the CTAs running at one
+// time share both their x and w tiles in L2.
+constexpr int kGroupM = 16;
+__device__ __forceinline__ void tile_coords(int64_t tile, int64_t num_m, int num_n, int64_t& mt, int& nt) {
+  const int64_t per_group = (int64_t)kGroupM * num_n;
+  const int64_t g = tile / per_group;
+  const int64_t in = tile - g * per_group;
+  const int64_t rows_here = min((int64_t)kGroupM, num_m - g * kGroupM);
+  mt = g * kGroupM + in % rows_here;
+  nt = (int)(in / rows_here);
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map), "r"(src),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     mxfp8_linear_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                        const uint8_t* __restrict__ sf_x, const uint8_t* __restrict__ sf_w,
-                        const float* __restrict__ inv_rms, uint16_t* __restrict__ out, int64_t T, int K, int N) {
+                        const __grid_constant__ CUtensorMap tm_out, const uint8_t* __restrict__ sf_x,
+                        const uint8_t* __restrict__ sf_w, const float* __restrict__ inv_rms, int64_t T, int K,
+                        int N) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kStageA;
   uint8_t* sSF = sB + kStages * kStageB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sSF + kStages * kStageSF);
+  uint8_t* sOut = sSF + kStages * kStageSF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 4 * kOutStage);
   // bars: full[kStages], empty[kStages], acc_full, acc_empty, drain; then the TMEM base word
   const uint32_t full0 = saddr(bars), empty0 = saddr(bars + kStages);
   const uint32_t acc_full = saddr(bars + 2 * kStages), acc_empty = saddr(bars + 2 * kStages + 1);
@@ -170,8 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t it = 0;
       bool ok = true;
       for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-        const int64_t mt = tile / num_n;
-        const int nt = (int)(tile % num_n);
+        int64_t mt;
+        int nt;
+        tile_coords(tile, num_m, num_n, mt, nt);
         for (int kt = 0; kt < num_kt; ++kt, ++it) {
           const int s = (int)(it % kStages);
           const uint32_t use = (uint32_t)(it / kStages);
@@ -231,46 +258,76 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int64_t rin = 32 * quad + lane;
+    uint8_t* stage = sOut + (warp - 2) * kOutStage;
+    const uint32_t stage_s = saddr(stage);
     int64_t tcount = 0;
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tcount) {
       if (!wait_bounded(acc_full, (uint32_t)(tcount & 1))) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int64_t row = (tile / num_n) * BM + rin;
-      const int n0 = (int)(tile % num_n) * BN;
-      const bool valid = row < T;
-      const float r = valid ? inv_rms[row] : 0.0f;
+      int64_t mt;
+      int nt;
+      tile_coords(tile, num_m, num_n, mt, nt);
+      const int64_t row0 = mt * BM + 32 * quad;
+      const int64_t row = row0 + lane;
+      const int n0 = nt * BN;
+      const float r = row < T ? inv_rms[row] : 0.0f;
       // Pull the whole 128 x 256 tile out of TMEM first (as packed bf16),
-      // hand TMEM back to the MMA issuer, then store: the next tile's MMAs
-      // run while these stores drain.
+      // four 32-column loads per wait, hand TMEM back to the MMA issuer,
+      // then store: the next tile's MMAs run while these stores drain.
       uint32_t o[BN / 2];
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t v[32];
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
-            "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
-              "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
-              "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-              "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-            : "r"(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)c0));
+      for (int h = 0; h < BN; h += 128) {
+        uint32_t v[128];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t* w = v + 32 * q;
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+              "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+              : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]), "=r"(w[8]),
+                "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]), "=r"(w[14]), "=r"(w[15]), "=r"(w[16]),
+                "=r"(w[17]), "=r"(w[18]), "=r"(w[19]), "=r"(w[20]), "=r"(w[21]), "=r"(w[22]), "=r"(w[23]), "=r"(w[24]),
+                "=r"(w[25]), "=r"(w[26]), "=r"(w[27]), "=r"(w[28]), "=r"(w[29]), "=r"(w[30]), "=r"(w[31])
+              : "r"(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(h + 32 * q)));
+        }
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 64; ++i) {
           const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), r),
                                                          __fmul_rn(__uint_as_float(v[2 * i + 1]), r));
-          o[c0 / 2 + i] = *reinterpret_cast<const uint32_t*>(&b);
+          o[h / 2 + i] = *reinterpret_cast<const uint32_t*>(&b);
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acc_empty) : "memory");
-      if (valid) {
-        uint16_t* orow = out + row * (int64_t)N + n0;
+      // Store the warp's 32 rows in 64-column boxes through a 4 KiB staging
+      // buffer in the 128-byte-swizzled layout the output tensor map uses
+      // (16-byte chunk j of row r at chunk j ^ (r % 8)); TMA clips rows >= T.
 #pragma unroll
-        for (int q = 0; q < BN / 8; ++q) stg16(orow + 8 * q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      for (int c = 0; c < BN; c += kOutChunk) {
+        if (c > 0 || tcount > 0) {
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t dst = stage_s + lane * 128 + ((j ^ (lane & 7)) * 16);
+          const int q = c / 2 + 4 * j;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(o[q]), "r"(o[q + 1]), "r"(o[q + 2]),
+                       "r"(o[q + 3])
+                       : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_out, stage_s, n0 + c, (int)row0);
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
       }
     }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
   }
 
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -294,6 +351,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// bf16 output [rows, N]: box of 32 rows x 64 columns (128 bytes), 128-byte swizzle
+bool encode_out(CUtensorMap* map, void* base, int64_t rows, int64_t N) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kOutChunk, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // rows x K uint8 codes, box of `box_rows` rows x 128 bytes, 128-byte swizzle
 bool encode_codes(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
   auto enc = tensor_map_encoder();
@@ -310,16 +379,17 @@ bool encode_codes(CUtensorMap* map, const void* base, int64_t rows, int64_t K, u
 }  // namespace
 
 cudaError_t launch_mxfp8_linear(const LinearArgs& a, cudaStream_t s) {
-  CUtensorMap tm_x, tm_w;
-  if (!encode_codes(&tm_x, a.x_codes, a.T, a.K, BM) || !encode_codes(&tm_w, a.w_codes, a.N, a.K, BN))
+  CUtensorMap tm_x, tm_w, tm_out;
+  if (!encode_codes(&tm_x, a.x_codes, a.T, a.K, BM) || !encode_codes(&tm_w, a.w_codes, a.N, a.K, BN) ||
+      !encode_out(&tm_out, a.out, a.T, a.N))
     return cudaErrorInvalidValue;
   const void* kern = reinterpret_cast<const void*>(mxfp8_linear_kernel);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (err != cudaSuccess) return err;
   const int64_t tiles = ((a.T + BM - 1) / BM) * (a.N / BN);
   const int grid = persistent_grid(kern, kThreads, tiles, kSmemBytes);
-  mxfp8_linear_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, a.x_scales, a.w_scales, a.inv_rms,
-                                                         static_cast<uint16_t*>(a.out), a.T, (int)a.K, (int)a.N);
+  mxfp8_linear_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, tm_out, a.x_scales, a.w_scales, a.inv_rms,
+                                                         a.T, (int)a.K, (int)a.N);
   return cudaGetLastError();
 }
 
