@@ -12,32 +12,47 @@
 // (mx_cast_fwd).  The row scale commutes with the matmul, so it is applied
 // once per output element in the epilogue.
 //
-// Tiling: 128 x 256 output tiles (one tcgen05.mma M = 128, N = 256 per
-// 32-element K step, cta_group::1, kind::mxf8f6f4 with 1X E8M0 block
-// scales), K staged 128 bytes at a time through a 4-deep shared-memory ring.
-// Persistent CTAs, one per SM, warp-specialised:
-//   warp 0 lane 0  TMA producer: 2-D tiled loads of the x and w code tiles
-//                  (128-byte swizzle) plus 1-D bulk copies of the 512-byte
-//                  scale atoms, completing on the stage's "full" mbarrier;
-//   warp 1 lane 0  MMA issuer: per stage, tcgen05.cp of the scale atoms
-//                  into TMEM (32 lanes x 128 bits, replicated to the 4 lane
-//                  quadrants), four tcgen05.mma, then tcgen05.commit to the
-//                  stage's "empty" mbarrier; after a tile's last stage a
-//                  commit to "acc_full";
-//   warps 2-5      epilogue: tcgen05.ld of the fp32 accumulators (each warp
-//                  its TMEM lane quadrant = 32 rows), times rho~[row],
-//                  rounded to packed bf16 in registers; "acc_empty" then
-//                  frees TMEM for the next tile's MMAs, and the rows leave
-//                  through per-warp 4 KiB swizzled staging buffers as TMA
-//                  tensor stores of 32 x 64 bf16 boxes.
-// TMEM: accumulators in columns 0-255, the scale factors of ring stage s in
+// Tiling: 256 x 256 output tiles, each computed by a pair of CTAs on the two
+// SMs of a TPC (a cluster of 2): tcgen05.mma with cta_group::2, M = 256
+// (128 rows per CTA), N = 256, kind::mxf8f6f4 with 1X E8M0 block scales, one
+// instruction per 32-element K step.  Each CTA stages its own 128 x rows and
+// one half (128 rows) of the tile's 256 w rows, K 128 bytes at a time
+// through a 6-deep shared-memory ring; the pair's tensor cores read both w
+// halves, so every w byte crosses L2 -> SM once per pair rather than once per
+// CTA.  Persistent pairs, warp-specialised (224 threads per CTA):
+//   warp 0 lane 0  TMA producer (both CTAs): 2-D tiled loads of the CTA's x
+//                  rows and w half (128-byte swizzle) and of the 512-byte
+//                  scale atoms (its own x atom, both w atoms), all completing
+//                  on the leader's stage "full" mbarrier (cta_group::2 form),
+//                  which expects both CTAs' bytes;
+//   warp 6 lane 0  leader CTA: scale-factor copier.  Per stage it waits for
+//                  "full", copies the atoms into both CTAs' TMEM (tcgen05.cp,
+//                  cta_group::2: each CTA's shared memory into its own TMEM)
+//                  and commits to "sf_full".  Copies issued by the MMA thread
+//                  itself would wait between its stages; from a thread of
+//                  their own they overlap the MMAs in flight;
+//   warp 1 lane 0  leader CTA: MMA issuer.  Per stage it waits for
+//                  "sf_full", issues four tcgen05.mma and commits to the
+//                  "empty" mbarriers of both CTAs (multicast); after a tile's
+//                  last stage it commits to both CTAs' "acc_full";
+//   warps 2-5      epilogue (both CTAs): tcgen05.ld of the CTA's fp32
+//                  accumulators (each warp its TMEM lane quadrant = 32 rows),
+//                  times rho~[row], rounded to packed bf16 in registers; an
+//                  arrival on the leader's "acc_empty" (8 per tile) frees
+//                  TMEM for the next tile's MMAs, and the rows leave through
+//                  per-warp 4 KiB swizzled staging buffers as TMA tensor
+//                  stores of 32 x 64 bf16 boxes.
+// Each CTA's tensor core reads the B scales of all 256 columns from its own
+// TMEM, so both CTAs load both w atoms.  TMEM (512 columns, allocated for the
+// pair): accumulators in columns 0-255, the scale factors of ring stage s in
 // columns 256 + 16 s (A: 4 columns, B: 8).  Every mbarrier wait is bounded
-// (2 s by %globaltimer); on expiry the waiter sets bit 1 of the device error
-// word and the kernel winds down, waiting (bounded) for its own bulk copies
-// and MMAs before it frees TMEM.
+// (2 s by %globaltimer); on expiry the waiter sets bit 0 of the linear error
+// word and the pair winds down, waiting (bounded) for its own bulk copies and
+// MMAs before it frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "launch.h"
@@ -49,12 +64,12 @@ __device__ unsigned int g_linear_error_word = 0u;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128;     // BK in bytes = E4M3 elements
-constexpr int kStages = 4;
+constexpr int BM = 128, BN = 256, BK = 128;     // BM rows per CTA (256 per pair); BK bytes = E4M3 elements
+constexpr int kStages = 6;
 constexpr int kStageA = BM * BK;                 // 16 KiB
-constexpr int kStageB = BN * BK;                 // 32 KiB
-constexpr int kStageSF = 512 + 2 * 512;          // one A scale atom, two B scale atoms
-constexpr int kThreads = 192;
+constexpr int kStageB = (BN / 2) * BK;           // 16 KiB: this CTA's half of the tile's w rows
+constexpr int kStageSF = 512 + 2 * 512;          // one A scale atom, both B scale atoms
+constexpr int kThreads = 224;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTxBytes = kStageA + kStageB + kStageSF;
 constexpr unsigned long long kWaitNs = 2000000000ull;
@@ -94,6 +109,25 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of either CTA.  The default (CTA-scope) release:
+// what the waiter needs ordered is the tcgen05 work fenced around the
+// barrier, and a cluster-scope release here costs microseconds per arrival.
+__device__ __forceinline__ void arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// All threads of both CTAs (per-thread form: callers may arrive diverged).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // K-major operand tile with 128-byte swizzle: 8-row atoms of 1024 bytes,
 // leading offset unused, stride 1024 bytes, descriptor version 1.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
@@ -108,11 +142,11 @@ __device__ __forceinline__ uint64_t desc_atom(uint32_t addr) {
 }
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling: E4M3 x E4M3,
-// both K-major, E8M0 scales, M = 128, N = 256, scale byte `sf` of each
-// 32-bit TMEM scale word for A and B (the 32-element K step within the
+// both K-major, E8M0 scales, M = 256 (the pair), N = 256, scale byte `sf` of
+// each 32-bit TMEM scale word for A and B (the 32-element K step within the
 // 128-element stage).
 __device__ __forceinline__ uint32_t idesc_mxf8(int sf) {
-  return ((uint32_t)sf << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24) |
+  return ((uint32_t)sf << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)((2 * BM) >> 4) << 24) |
          ((uint32_t)sf << 29);
 }
 
@@ -123,15 +157,20 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
       : "memory");
 }
 
-__device__ __forceinline__ void bulk_512(uint32_t dst, const void* src, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 512, [%2];" ::"r"(dst),
-               "l"(src), "r"(bar)
-               : "memory");
+// The same, completing on an mbarrier of either CTA of the pair (bar: a
+// shared::cluster address), so the peer's loads count towards the leader's
+// stage barrier directly.
+__device__ __forceinline__ void tma_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
 
-// Persistent tile order: groups of kGroupM row tiles walk the column tiles
-// together (row tile fastest inside a group), so the CTAs running at one
-// time share both their x and w tiles in L2.
+// Persistent tile order: groups of kGroupM 256-row tiles walk the column
+// tiles together (row tile fastest inside a group), so the pairs running at
+// one time share both their x and w tiles in L2.
 constexpr int kGroupM = 16;
 __device__ __forceinline__ void tile_coords(int64_t tile, int64_t num_m, int num_n, int64_t& mt, int& nt) {
   const int64_t per_group = (int64_t)kGroupM * num_n;
@@ -148,11 +187,11 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mxfp8_linear_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                        const __grid_constant__ CUtensorMap tm_out, const uint8_t* __restrict__ sf_x,
-                        const uint8_t* __restrict__ sf_w, const float* __restrict__ inv_rms, int64_t T, int K,
-                        int N) {
+                        const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_sfx,
+                        const __grid_constant__ CUtensorMap tm_sfw, const float* __restrict__ inv_rms, int64_t T,
+                        int K, int N) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -160,34 +199,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sSF = sB + kStages * kStageB;
   uint8_t* sOut = sSF + kStages * kStageSF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 4 * kOutStage);
-  // bars: full[kStages], empty[kStages], acc_full, acc_empty, drain; then the TMEM base word
-  const uint32_t full0 = saddr(bars), empty0 = saddr(bars + kStages);
-  const uint32_t acc_full = saddr(bars + 2 * kStages), acc_empty = saddr(bars + 2 * kStages + 1);
-  const uint32_t drain = saddr(bars + 2 * kStages + 2);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 3);
+  // bars: full[kStages], empty[kStages], sf_full[kStages], acc_full, acc_empty, drain, drain_sf;
+  // then the TMEM base word.  The leader's full[s] counts both CTAs' bytes; the peer uses only
+  // empty[] and acc_full.
+  const uint32_t full0 = saddr(bars), empty0 = saddr(bars + kStages), sf_full0 = saddr(bars + 2 * kStages);
+  const uint32_t acc_full = saddr(bars + 3 * kStages), acc_empty = saddr(bars + 3 * kStages + 1);
+  const uint32_t drain = saddr(bars + 3 * kStages + 2), drain_sf = saddr(bars + 3 * kStages + 3);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int num_n = N / BN, num_kt = K / BK;
-  const int64_t num_m = (T + BM - 1) / BM;
+  const int64_t num_m = (T + 2 * BM - 1) / (2 * BM);  // 256-row tiles
+  const int64_t row_atoms = (T + BM - 1) / BM;          // 128-row scale atoms of x
   const int64_t tiles = num_m * num_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(full0 + 8 * s));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * s));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sf_full0 + 8 * s));
     }
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(acc_full));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(acc_empty));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(acc_empty));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(drain));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(drain_sf));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
+  if (warp == 1) {  // one warp of each CTA allocates the pair's TMEM together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
                  "r"(kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // both CTAs' barriers are initialised before either arrives remotely
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
@@ -195,85 +243,132 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int64_t it = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      for (int64_t tile = pair; tile < tiles && ok; tile += npairs) {
         int64_t mt;
         int nt;
         tile_coords(tile, num_m, num_n, mt, nt);
+        const int64_t xrow = (2 * mt + rank) * BM;
+        // rows past T load as zeros (TMA); their scale atom is any valid one
+        const int64_t xatom = min(2 * mt + (int64_t)rank, row_atoms - 1);
         for (int kt = 0; kt < num_kt; ++kt, ++it) {
           const int s = (int)(it % kStages);
           const uint32_t use = (uint32_t)(it / kStages);
           if (use > 0 && !(ok = wait_bounded(empty0 + 8 * s, (use - 1) & 1u))) break;
-          const uint32_t fb = full0 + 8 * s;
-          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(kTxBytes) : "memory");
-          tma_2d(saddr(sA + s * kStageA), &tm_x, kt * BK, (int)(mt * BM), fb);
-          tma_2d(saddr(sB + s * kStageB), &tm_w, kt * BK, nt * BN, fb);
-          uint8_t* sf = sSF + s * kStageSF;
-          bulk_512(saddr(sf), sf_x + (mt * num_kt + kt) * 512, fb);
-          bulk_512(saddr(sf + 512), sf_w + ((int64_t)(2 * nt) * num_kt + kt) * 512, fb);
-          bulk_512(saddr(sf + 1024), sf_w + ((int64_t)(2 * nt + 1) * num_kt + kt) * 512, fb);
+          const uint32_t fb = map_to_rank(full0 + 8 * s, 0);  // the leader's stage barrier
+          if (rank == 0)
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full0 + 8 * s), "r"(2 * kTxBytes)
+                         : "memory");
+          tma_2d_pair(saddr(sA + s * kStageA), &tm_x, kt * BK, (int)xrow, fb);
+          tma_2d_pair(saddr(sB + s * kStageB), &tm_w, kt * BK, nt * BN + (int)rank * (BN / 2), fb);
+          // scale atoms: 512 bytes = 4 rows of the 128-byte-wide scale maps
+          const uint32_t sf = saddr(sSF + s * kStageSF);
+          tma_2d_pair(sf, &tm_sfx, 0, (int)(4 * (xatom * num_kt + kt)), fb);
+          tma_2d_pair(sf + 512, &tm_sfw, 0, (int)(4 * ((int64_t)(2 * nt) * num_kt + kt)), fb);
+          tma_2d_pair(sf + 1024, &tm_sfw, 0, (int)(4 * ((int64_t)(2 * nt + 1) * num_kt + kt)), fb);
         }
       }
-      // every copy issued must have landed before the CTA may exit
-      for (int64_t i = (it > kStages ? it - kStages : 0); i < it; ++i)
-        (void)wait_bounded(full0 + 8 * (int)(i % kStages), (uint32_t)(i / kStages) & 1u);
+      // every copy issued (both CTAs') must have landed before the pair may
+      // exit: the leader waits for its barriers' last phases
+      if (rank == 0)
+        for (int64_t i = (it > kStages ? it - kStages : 0); i < it; ++i)
+          (void)wait_bounded(full0 + 8 * (int)(i % kStages), (uint32_t)(i / kStages) & 1u);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int64_t it = 0, tcount = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++tcount) {
+      for (int64_t tile = pair; tile < tiles && ok; tile += npairs, ++tcount) {
         if (tcount > 0 && !(ok = wait_bounded(acc_empty, (uint32_t)((tcount - 1) & 1)))) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         for (int kt = 0; kt < num_kt; ++kt, ++it) {
           const int s = (int)(it % kStages);
-          if (!(ok = wait_bounded(full0 + 8 * s, (uint32_t)(it / kStages) & 1u))) break;
+          // the stage's operands have landed and its scale factors are in TMEM
+          if (!(ok = wait_bounded(sf_full0 + 8 * s, (uint32_t)(it / kStages) & 1u))) break;
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
           const uint32_t tsf = tmem + 256 + 16 * s;
-          const uint32_t sf = saddr(sSF + s * kStageSF);
-          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsf), "l"(desc_atom(sf)));
-          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 4), "l"(desc_atom(sf + 512)));
-          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 8), "l"(desc_atom(sf + 1024)));
           const uint32_t a0 = saddr(sA + s * kStageA), b0 = saddr(sB + s * kStageB);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t accum = (kt | j) ? 1u : 0u;
             asm volatile(
                 "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
-                "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
                     tmem),
                 "l"(desc_sw128(a0 + 32 * j)), "l"(desc_sw128(b0 + 32 * j)), "r"(idesc_mxf8(j)), "r"(tsf), "r"(tsf + 4),
                 "r"(accum));
           }
-          asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty0 + 8 * s)
-                       : "memory");
+          asm volatile(
+              "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                  empty0 + 8 * s),
+              "h"((uint16_t)3)
+              : "memory");
         }
         if (!ok) break;
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(acc_full)
-                     : "memory");
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                acc_full),
+            "h"((uint16_t)3)
+            : "memory");
       }
       // all MMAs and scale copies of this thread complete before TMEM is freed
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(drain) : "memory");
+      asm volatile(
+          "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+              drain),
+          "h"((uint16_t)1)
+          : "memory");
       (void)wait_bounded(drain, 0);
+    }
+  } else if (warp == 6) {
+    if (lane == 0 && rank == 0) {
+      // Scale-factor copier: tcgen05.cp from a thread of its own, so the
+      // copies overlap the MMAs in flight (issued from the MMA thread they
+      // wait, in order, between its stages).  Slot s of TMEM is free again
+      // once full[s] shows the next use of stage s: the producer refilled it
+      // only after the MMAs that read the slot completed.
+      const int64_t my_tiles = pair < tiles ? (tiles - 1 - pair) / npairs + 1 : 0;
+      const int64_t total = my_tiles * num_kt;
+      for (int64_t it = 0; it < total; ++it) {
+        const int s = (int)(it % kStages);
+        if (!wait_bounded(full0 + 8 * s, (uint32_t)(it / kStages) & 1u)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t tsf = tmem + 256 + 16 * s;
+        const uint32_t sf = saddr(sSF + s * kStageSF);
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf), "l"(desc_atom(sf)));
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 4), "l"(desc_atom(sf + 512)));
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 8), "l"(desc_atom(sf + 1024)));
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                sf_full0 + 8 * s),
+            "h"((uint16_t)1)
+            : "memory");
+      }
+      // its copies complete before TMEM is freed
+      asm volatile(
+          "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+              drain_sf),
+          "h"((uint16_t)1)
+          : "memory");
+      (void)wait_bounded(drain_sf, 0);
     }
   } else {
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
-    const int64_t rin = 32 * quad + lane;
     uint8_t* stage = sOut + (warp - 2) * kOutStage;
     const uint32_t stage_s = saddr(stage);
+    const uint32_t acc_empty_leader = map_to_rank(acc_empty, 0);
     int64_t tcount = 0;
-    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tcount) {
+    for (int64_t tile = pair; tile < tiles; tile += npairs, ++tcount) {
       if (!wait_bounded(acc_full, (uint32_t)(tcount & 1))) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       int64_t mt;
       int nt;
       tile_coords(tile, num_m, num_n, mt, nt);
-      const int64_t row0 = mt * BM + 32 * quad;
+      const int64_t row0 = (2 * mt + rank) * BM + 32 * quad;
       const int64_t row = row0 + lane;
       const int n0 = nt * BN;
       const float r = row < T ? inv_rms[row] : 0.0f;
-      // Pull the whole 128 x 256 tile out of TMEM first (as packed bf16),
-      // four 32-column loads per wait, hand TMEM back to the MMA issuer,
-      // then store: the next tile's MMAs run while these stores drain.
+      // Pull the CTA's whole 128 x 256 share out of TMEM first (as packed
+      // bf16), four 32-column loads per wait, hand TMEM back to the MMA
+      // issuer, then store: the next tile's MMAs run while these drain.
       uint32_t o[BN / 2];
 #pragma unroll
       for (int h = 0; h < BN; h += 128) {
@@ -300,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
-      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acc_empty) : "memory");
+      if (lane == 0) arrive_remote(acc_empty_leader);
       // Store the warp's 32 rows in 64-column boxes through a 4 KiB staging
       // buffer in the 128-byte-swizzled layout the output tensor map uses
       // (16-byte chunk j of row r at chunk j ^ (r % 8)); TMA clips rows >= T.
@@ -330,11 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
 
+  // Neither CTA leaves (or frees TMEM) while the pair's MMAs may still read
+  // its shared memory or the other CTA may still arrive on its barriers.
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
+  __syncwarp();
+  cluster_sync();
   if (warp == 1) {
+    __syncwarp();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
   }
 }
 
@@ -376,19 +475,70 @@ bool encode_codes(CUtensorMap* map, const void* base, int64_t rows, int64_t K, u
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// CTA pairs of the kernel that the current device runs at the same time
+// (clusters stay inside one GPC, so this can be below SMs / 2), cached per
+// device.
+cudaError_t resident_pairs(const void* kern, int* out) {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+    *out = cache[dev];
+    return cudaSuccess;
+  }
+  int sms = 0;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(sms - sms % 2));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  int clusters = 0;
+  if ((err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg)) != cudaSuccess) return err;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  if (dev >= 0 && dev < 64) cache[dev] = clusters;
+  *out = clusters;
+  return cudaSuccess;
+}
+
+// MMA-layout scale bytes viewed as rows of 128 bytes (a 512-byte atom is 4
+// rows), box of 4 rows, no swizzle: one TMA load per atom.
+bool encode_scales(CUtensorMap* map, const void* base, int64_t bytes) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)(bytes / 128)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, 4};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_mxfp8_linear(const LinearArgs& a, cudaStream_t s) {
-  CUtensorMap tm_x, tm_w, tm_out;
-  if (!encode_codes(&tm_x, a.x_codes, a.T, a.K, BM) || !encode_codes(&tm_w, a.w_codes, a.N, a.K, BN) ||
-      !encode_out(&tm_out, a.out, a.T, a.N))
+  CUtensorMap tm_x, tm_w, tm_out, tm_sfx, tm_sfw;
+  const int64_t sfx_bytes = ((a.T + BM - 1) / BM) * (a.K / BK) * 512;
+  const int64_t sfw_bytes = ((a.N + BM - 1) / BM) * (a.K / BK) * 512;
+  if (!encode_codes(&tm_x, a.x_codes, a.T, a.K, BM) || !encode_codes(&tm_w, a.w_codes, a.N, a.K, BN / 2) ||
+      !encode_out(&tm_out, a.out, a.T, a.N) || !encode_scales(&tm_sfx, a.x_scales, sfx_bytes) ||
+      !encode_scales(&tm_sfw, a.w_scales, sfw_bytes))
     return cudaErrorInvalidValue;
   const void* kern = reinterpret_cast<const void*>(mxfp8_linear_kernel);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (err != cudaSuccess) return err;
-  const int64_t tiles = ((a.T + BM - 1) / BM) * (a.N / BN);
-  const int grid = persistent_grid(kern, kThreads, tiles, kSmemBytes);
-  mxfp8_linear_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, tm_out, a.x_scales, a.w_scales, a.inv_rms,
+  int co_resident = 0;
+  if ((err = resident_pairs(kern, &co_resident)) != cudaSuccess) return err;
+  // persistent pairs: as many as can run at once (a pair that waited for a
+  // second wave would start its share of tiles only after the first wave
+  // finished), never more than tiles
+  const int64_t tiles = ((a.T + 2 * BM - 1) / (2 * BM)) * (a.N / BN);
+  const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(tiles, co_resident));
+  const int grid = (int)(2 * pairs);
+  mxfp8_linear_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, tm_out, tm_sfx, tm_sfw, a.inv_rms,
                                                          a.T, (int)a.K, (int)a.N);
   return cudaGetLastError();
 }

@@ -125,6 +125,17 @@ def test_linear_llama3_8b_layer_sampled():
     linear_case(T, 4096, 4096, seed=9, rows=rows)
 
 
+def test_linear_many_tiles_per_pair_sampled():
+    """Several 256 x 256 tiles per persistent CTA pair (33 row tiles x 16
+    column tiles), so the accumulator hand-off between the pair's epilogue
+    and its MMA issuer runs through many phases; sampled rows of every row
+    tile, the ragged last one included."""
+    T = 8192 + 77
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([np.arange(0, T, 251), np.arange(T - 4, T), rng.integers(0, T, 8)]))
+    linear_case(T, 1024, 4096, seed=11, rows=rows)
+
+
 def test_linear_no_device_error_flag():
     linear_case(256, 512, 256, seed=1)
     assert mx.device_errors() == 0
