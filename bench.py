@@ -306,19 +306,57 @@ def run_gpu(args):
         if st:
             raise RuntimeError(mx.lib().mxnorm_last_error().decode())
 
+    # A library yardstick for the hand-written GEMM: cuBLASLt's MXFP8
+    # block-scaled GEMM (torch._scaled_mm with E8M0 scales, which take the
+    # same tcgen05 scale layout) on the same codes, timed the same way in
+    # alternating blocks so that neither runs only in the other's power and
+    # clock wake.  Its output lacks the inv_rms epilogue; against our kernel
+    # run with inv_rms = 1 it is compared bit for bit.
+    a8, b8 = xq_codes.view(torch.float8_e4m3fn), w_codes.view(torch.float8_e4m3fn)
+
+    def cublas_step(i):
+        torch._scaled_mm(a8, b8.t(), scale_a=xq_scales.view(torch.float8_e8m0fnu),
+                         scale_b=w_scales.view(torch.float8_e8m0fnu), out_dtype=torch.bfloat16)
+
     perq, _ = time_launches(torch, stream, quant_mma_step, sec_steps, 5, nbuf)
-    lin_steps = max(10, sec_steps // 10)
-    perl, _ = time_launches(torch, stream, linear_step, lin_steps, 3, nbuf)
+    lin_steps = max(10, sec_steps // 20)
+    perl, perc, cublas_note = [], [], None
+    for _ in range(2):
+        perl += time_launches(torch, stream, linear_step, lin_steps, 3, nbuf)[0]
+        if cublas_note is None:
+            try:
+                perc += time_launches(torch, stream, cublas_step, lin_steps, 3, nbuf)[0]
+            except Exception as e:  # no MX support in this torch / cuBLASLt
+                cublas_note = f"unavailable: {type(e).__name__}: {str(e)[:160]}"
     mq, ml = statistics.fmean(perq), statistics.fmean(perl)
     fp8_peak = 2.0 * float(peaks.get("bf16_tflops", 1900.0))
     tflops = 2.0 * T * H * Nw / (ml * 1e-3) / 1e12
     extra["mxnorm_quant_mma_layout_p2"] = {"ms": round(mq, 5), "GB/s": gbs(abytes, mq),
                                            "frac": round(gbs(abytes, mq) / hbm_peak, 4)}
-    extra["mxnorm_linear_fwd_65536x4096x4096"] = {
+    lin = extra["mxnorm_linear_fwd_65536x4096x4096"] = {
         "ms": round(ml, 5), "TFLOP/s": round(tflops, 1), "frac_of_fp8_peak": round(tflops / fp8_peak, 4),
         "fp8_peak_TFLOPs": round(fp8_peak, 1), "peak_source": f"{peak_kind} bf16_tflops x 2 (fp8/bf16 nominal)",
         "layer_tokens_per_s": round(T / ((mq + ml) * 1e-3), 1)}
-    del w_codes, w_scales, xq_codes, xq_scales, xq_inv, lin_out
+    if cublas_note is None:
+        mc = statistics.fmean(perc)
+        tc = 2.0 * T * H * Nw / (mc * 1e-3) / 1e12
+        ones = torch.ones_like(xq_inv)
+        with torch.cuda.stream(stream):
+            ref = torch._scaled_mm(a8, b8.t(), scale_a=xq_scales.view(torch.float8_e8m0fnu),
+                                   scale_b=w_scales.view(torch.float8_e8m0fnu), out_dtype=torch.bfloat16)
+            st = mx.lib().mxnorm_linear_fwd(xq_codes.data_ptr(), xq_scales.data_ptr(), ones.data_ptr(),
+                                            w_codes.data_ptr(), w_scales.data_ptr(), T, H, Nw, lin_out.data_ptr(),
+                                            ctypes.c_void_p(sptr))
+        torch.cuda.synchronize()
+        if st:
+            raise RuntimeError(mx.lib().mxnorm_last_error().decode())
+        lin["cublaslt_mxfp8_same_inputs"] = {
+            "ms": round(mc, 5), "TFLOP/s": round(tc, 1), "ours_over_cublaslt": round(tflops / tc, 4),
+            "bit_equal_with_inv_rms_1": bool(torch.equal(ref, lin_out))}
+        del ref, ones
+    else:
+        lin["cublaslt_mxfp8_same_inputs"] = cublas_note
+    del w_codes, w_scales, xq_codes, xq_scales, xq_inv, lin_out, a8, b8
 
     y_ws = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
 
@@ -476,6 +514,26 @@ def run_profile_case(args):
     T, H = args.profile_rows, w.H
     x = torch.from_numpy(synth.make_activations(w, rows=T).view(np.int16)).view(torch.bfloat16).cuda()
     stream = torch.cuda.Stream()
+    if args.profile_linear:
+        # MXNormLinear's GEMM: the rows quantised with MMA-layout scales
+        # against a 4096 x 4096 MXFP8 weight (a Llama-3-8B projection)
+        Nw = 4096
+        gw = torch.Generator(device="cuda").manual_seed(7)
+        wt = (torch.randn((Nw, H), device="cuda", generator=gw) * 0.02).to(torch.bfloat16)
+        w_codes, w_scales = mx.mx_cast(wt, "mma")
+        xc, xs, xinv = mx.quant_fwd_mma(x, 2, "mxfp8")
+        out = torch.empty((T, Nw), dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()
+
+        def fn_lin(i):
+            mx.linear_fwd(xc, xs, xinv, w_codes, w_scales, out=out, stream=stream)
+        per, region = time_launches(torch, stream, fn_lin, args.steps, args.warmup, 1)
+        m = statistics.fmean(per)
+        print(json.dumps({"profile_only": True, "kernel": "mxnorm_linear_fwd", "T": T, "K": H, "N": Nw,
+                          "mean_launch_ms": round(m, 6),
+                          "TFLOP/s": round(2.0 * T * H * Nw / (m * 1e-3) / 1e12, 1),
+                          "device_errors": mx.device_errors()}), flush=True)
+        return
     if args.profile_baseline:
         y = torch.empty_like(x)
 
@@ -514,6 +572,9 @@ def main():
     ap.add_argument("--profile-fmt", default="mxfp8", choices=["mxfp8", "mxfp4_h16"])
     ap.add_argument("--profile-baseline", action="store_true",
                     help="profiling case: the two-pass baseline instead of MXNorm")
+    ap.add_argument("--profile-linear", action="store_true",
+                    help="profiling case: MXNormLinear's GEMM (mxnorm_linear_fwd) on the first N rows "
+                         "against a 4096 x 4096 weight")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

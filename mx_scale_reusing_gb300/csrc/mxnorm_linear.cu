@@ -69,14 +69,12 @@ constexpr int kStages = 6;
 constexpr int kStageA = BM * BK;                 // 16 KiB
 constexpr int kStageB = (BN / 2) * BK;           // 16 KiB: this CTA's half of the tile's w rows
 constexpr int kStageSF = 512 + 2 * 512;          // one A scale atom, both B scale atoms
-constexpr int kThreads = 224;
+constexpr int kEpiWarps = 8;                     // two per TMEM lane quadrant, 128 columns each
+constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTxBytes = kStageA + kStageB + kStageSF;
+constexpr uint32_t kTxBytes = kStageA + kStageB + kStageSF;  // one CTA's bytes per stage
 constexpr unsigned long long kWaitNs = 2000000000ull;
-constexpr int kOutChunk = 64;                    // bf16 columns per TMA store box (128 bytes)
-constexpr int kOutStage = 32 * kOutChunk * 2;    // one epilogue warp's 32-row staging buffer, 4 KiB
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * (kStageA + kStageB + kStageSF) +
-                              4 * kOutStage + 256;
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * (kStageA + kStageB + kStageSF) + 256;
 
 __device__ __forceinline__ uint32_t saddr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -150,16 +148,9 @@ __device__ __forceinline__ uint32_t idesc_mxf8(int sf) {
          ((uint32_t)sf << 29);
 }
 
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// The same, completing on an mbarrier of either CTA of the pair (bar: a
-// shared::cluster address), so the peer's loads count towards the leader's
-// stage barrier directly.
+// 2-D tiled TMA load into this CTA's shared memory, completing on an
+// mbarrier of either CTA of the pair (bar: a shared::cluster address), so
+// the peer's loads count towards the leader's stage barrier directly.
 __device__ __forceinline__ void tma_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, "
@@ -181,24 +172,69 @@ __device__ __forceinline__ void tile_coords(int64_t tile, int64_t num_m, int num
   nt = (int)(in / rows_here);
 }
 
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map), "r"(src),
-               "r"(x), "r"(y)
-               : "memory");
+
+// One lane's 128 consecutive bf16 outputs (64 packed words) to global
+// memory: 32-byte stores (whole sectors) when the row start allows, else
+// 16-byte ones.
+template <bool kV8>
+__device__ __forceinline__ void store_row128(uint16_t* dst, const uint32_t (&o)[64]) {
+#pragma unroll
+  for (int q = 0; q < 64; q += 8) {
+    if constexpr (kV8) {
+      asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 2 * q), "r"(o[q]), "r"(o[q + 1]),
+                   "r"(o[q + 2]), "r"(o[q + 3]), "r"(o[q + 4]), "r"(o[q + 5]), "r"(o[q + 6]), "r"(o[q + 7])
+                   : "memory");
+    } else {
+      asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(dst + 2 * q), "r"(o[q]), "r"(o[q + 1]), "r"(o[q + 2]),
+                   "r"(o[q + 3])
+                   : "memory");
+      asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(dst + 2 * q + 8), "r"(o[q + 4]), "r"(o[q + 5]),
+                   "r"(o[q + 6]), "r"(o[q + 7])
+                   : "memory");
+    }
+  }
 }
 
+// 64 TMEM columns of this warp's 32 lanes (two 32-column loads, completed
+// by the caller's tcgen05.wait::ld).
+__device__ __forceinline__ void tmem_load64(uint32_t taddr, uint32_t (&v)[64]) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    uint32_t* w = v + 32 * q;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]), "=r"(w[8]),
+          "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]), "=r"(w[14]), "=r"(w[15]), "=r"(w[16]),
+          "=r"(w[17]), "=r"(w[18]), "=r"(w[19]), "=r"(w[20]), "=r"(w[21]), "=r"(w[22]), "=r"(w[23]), "=r"(w[24]),
+          "=r"(w[25]), "=r"(w[26]), "=r"(w[27]), "=r"(w[28]), "=r"(w[29]), "=r"(w[30]), "=r"(w[31])
+        : "r"(taddr + (uint32_t)(32 * q)));
+  }
+}
+
+// v * r in fp32 (IEEE products), rounded to bf16 and packed in pairs.
+__device__ __forceinline__ void scale_pack64(const uint32_t (&v)[64], float r, uint32_t* o) {
+  const unsigned long long rr = f2_pack(r, r);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float lo, hi;
+    f2_unpack(f2_mul(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), rr), lo, hi);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    o[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+}
+
+template <bool kV8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mxfp8_linear_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                        const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_sfx,
-                        const __grid_constant__ CUtensorMap tm_sfw, const float* __restrict__ inv_rms, int64_t T,
-                        int K, int N) {
+                        const __grid_constant__ CUtensorMap tm_sfx, const __grid_constant__ CUtensorMap tm_sfw,
+                        const float* __restrict__ inv_rms, uint16_t* __restrict__ out, int64_t T, int K, int N) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kStageA;
   uint8_t* sSF = sB + kStages * kStageB;
-  uint8_t* sOut = sSF + kStages * kStageSF;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 4 * kOutStage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSF + kStages * kStageSF);
   // bars: full[kStages], empty[kStages], sf_full[kStages], acc_full, acc_empty, drain, drain_sf;
   // then the TMEM base word.  The leader's full[s] counts both CTAs' bytes; the peer uses only
   // empty[] and acc_full.
@@ -223,7 +259,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sf_full0 + 8 * s));
     }
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(acc_full));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(acc_empty));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(acc_empty), "r"(2 * kEpiWarps));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(drain));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(drain_sf));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -318,7 +354,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           : "memory");
       (void)wait_bounded(drain, 0);
     }
-  } else if (warp == 6) {
+  } else if (warp == 2) {
     if (lane == 0 && rank == 0) {
       // Scale-factor copier: tcgen05.cp from a thread of its own, so the
       // copies overlap the MMAs in flight (issued from the MMA thread they
@@ -351,9 +387,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       (void)wait_bounded(drain_sf, 0);
     }
   } else {
-    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
-    uint8_t* stage = sOut + (warp - 2) * kOutStage;
-    const uint32_t stage_s = saddr(stage);
+    // Epilogue warps 3 .. 3 + kEpiWarps - 1: TMEM lane quadrant warp % 4
+    // (the lanes a warp may access), columns 128 * half .. + 128.
+    const int quad = warp & 3;
+    const int half = (warp - 3) / 4;
     const uint32_t acc_empty_leader = map_to_rank(acc_empty, 0);
     int64_t tcount = 0;
     for (int64_t tile = pair; tile < tiles; tile += npairs, ++tcount) {
@@ -362,67 +399,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int64_t mt;
       int nt;
       tile_coords(tile, num_m, num_n, mt, nt);
-      const int64_t row0 = (2 * mt + rank) * BM + 32 * quad;
-      const int64_t row = row0 + lane;
-      const int n0 = nt * BN;
+      const int64_t row = (2 * mt + rank) * BM + 32 * quad + lane;
+      const int c0 = nt * BN + 128 * half;
       const float r = row < T ? inv_rms[row] : 0.0f;
-      // Pull the CTA's whole 128 x 256 share out of TMEM first (as packed
-      // bf16), four 32-column loads per wait, hand TMEM back to the MMA
-      // issuer, then store: the next tile's MMAs run while these drain.
-      uint32_t o[BN / 2];
-#pragma unroll
-      for (int h = 0; h < BN; h += 128) {
-        uint32_t v[128];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t* w = v + 32 * q;
-          asm volatile(
-              "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-              "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-              : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]), "=r"(w[8]),
-                "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]), "=r"(w[14]), "=r"(w[15]), "=r"(w[16]),
-                "=r"(w[17]), "=r"(w[18]), "=r"(w[19]), "=r"(w[20]), "=r"(w[21]), "=r"(w[22]), "=r"(w[23]), "=r"(w[24]),
-                "=r"(w[25]), "=r"(w[26]), "=r"(w[27]), "=r"(w[28]), "=r"(w[29]), "=r"(w[30]), "=r"(w[31])
-              : "r"(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(h + 32 * q)));
-        }
+      const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(128 * half);
+      // Read the warp's 32 x 128 share of the accumulators, then hand TMEM
+      // back to the MMA issuer before the second half is converted and the
+      // row is stored: the next tile's MMAs overlap both.
+      uint32_t o[64];
+      {
+        uint32_t v[64];
+        tmem_load64(taddr, v);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), r),
-                                                         __fmul_rn(__uint_as_float(v[2 * i + 1]), r));
-          o[h / 2 + i] = *reinterpret_cast<const uint32_t*>(&b);
-        }
+        scale_pack64(v, r, o);
       }
+      uint32_t v[64];
+      tmem_load64(taddr + 64, v);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) arrive_remote(acc_empty_leader);
-      // Store the warp's 32 rows in 64-column boxes through a 4 KiB staging
-      // buffer in the 128-byte-swizzled layout the output tensor map uses
-      // (16-byte chunk j of row r at chunk j ^ (r % 8)); TMA clips rows >= T.
-#pragma unroll
-      for (int c = 0; c < BN; c += kOutChunk) {
-        if (c > 0 || tcount > 0) {
-          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-          __syncwarp();
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t dst = stage_s + lane * 128 + ((j ^ (lane & 7)) * 16);
-          const int q = c / 2 + 4 * j;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(o[q]), "r"(o[q + 1]), "r"(o[q + 2]),
-                       "r"(o[q + 3])
-                       : "memory");
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tm_out, stage_s, n0 + c, (int)row0);
-          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        }
-      }
+      scale_pack64(v, r, o + 32);
+      if (row < T) store_row128<kV8>(out + row * (int64_t)N + c0, o);
     }
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-    __syncwarp();
   }
 
   // Neither CTA leaves (or frees TMEM) while the pair's MMAs may still read
@@ -450,18 +449,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// bf16 output [rows, N]: box of 32 rows x 64 columns (128 bytes), 128-byte swizzle
-bool encode_out(CUtensorMap* map, void* base, int64_t rows, int64_t N) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)N * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kOutChunk, 32};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // rows x K uint8 codes, box of `box_rows` rows x 128 bytes, 128-byte swizzle
 bool encode_codes(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
   auto enc = tensor_map_encoder();
@@ -478,15 +465,15 @@ bool encode_codes(CUtensorMap* map, const void* base, int64_t rows, int64_t K, u
 // CTA pairs of the kernel that the current device runs at the same time
 // (clusters stay inside one GPC, so this can be below SMs / 2), cached per
 // device.
-cudaError_t resident_pairs(const void* kern, int* out) {
+cudaError_t resident_pairs(const void* kern, int variant, int* out) {
   static std::mutex mu;
-  static int cache[64] = {0};
+  static int cache[2][64] = {{0}};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   std::lock_guard<std::mutex> lock(mu);
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) {
-    *out = cache[dev];
+  if (dev >= 0 && dev < 64 && cache[variant][dev] > 0) {
+    *out = cache[variant][dev];
     return cudaSuccess;
   }
   int sms = 0;
@@ -498,7 +485,7 @@ cudaError_t resident_pairs(const void* kern, int* out) {
   int clusters = 0;
   if ((err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg)) != cudaSuccess) return err;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
-  if (dev >= 0 && dev < 64) cache[dev] = clusters;
+  if (dev >= 0 && dev < 64) cache[variant][dev] = clusters;
   *out = clusters;
   return cudaSuccess;
 }
@@ -520,26 +507,35 @@ bool encode_scales(CUtensorMap* map, const void* base, int64_t bytes) {
 }  // namespace
 
 cudaError_t launch_mxfp8_linear(const LinearArgs& a, cudaStream_t s) {
-  CUtensorMap tm_x, tm_w, tm_out, tm_sfx, tm_sfw;
+  CUtensorMap tm_x, tm_w, tm_sfx, tm_sfw;
   const int64_t sfx_bytes = ((a.T + BM - 1) / BM) * (a.K / BK) * 512;
   const int64_t sfw_bytes = ((a.N + BM - 1) / BM) * (a.K / BK) * 512;
   if (!encode_codes(&tm_x, a.x_codes, a.T, a.K, BM) || !encode_codes(&tm_w, a.w_codes, a.N, a.K, BN / 2) ||
-      !encode_out(&tm_out, a.out, a.T, a.N) || !encode_scales(&tm_sfx, a.x_scales, sfx_bytes) ||
+      !encode_scales(&tm_sfx, a.x_scales, sfx_bytes) ||
       !encode_scales(&tm_sfw, a.w_scales, sfw_bytes))
     return cudaErrorInvalidValue;
-  const void* kern = reinterpret_cast<const void*>(mxfp8_linear_kernel);
+  // rows start 32-byte aligned when out is (N is a multiple of 256)
+  const bool v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
+  const void* kern = v8 ? reinterpret_cast<const void*>(mxfp8_linear_kernel<true>)
+                        : reinterpret_cast<const void*>(mxfp8_linear_kernel<false>);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (err != cudaSuccess) return err;
   int co_resident = 0;
-  if ((err = resident_pairs(kern, &co_resident)) != cudaSuccess) return err;
+  if ((err = resident_pairs(kern, v8 ? 0 : 1, &co_resident)) != cudaSuccess) return err;
   // persistent pairs: as many as can run at once (a pair that waited for a
   // second wave would start its share of tiles only after the first wave
   // finished), never more than tiles
   const int64_t tiles = ((a.T + 2 * BM - 1) / (2 * BM)) * (a.N / BN);
   const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(tiles, co_resident));
   const int grid = (int)(2 * pairs);
-  mxfp8_linear_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, tm_out, tm_sfx, tm_sfw, a.inv_rms,
-                                                         a.T, (int)a.K, (int)a.N);
+  if (v8)
+    mxfp8_linear_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, tm_sfx, tm_sfw, a.inv_rms,
+                                                                 static_cast<uint16_t*>(a.out), a.T, (int)a.K,
+                                                                 (int)a.N);
+  else
+    mxfp8_linear_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, tm_sfx, tm_sfw, a.inv_rms,
+                                                                  static_cast<uint16_t*>(a.out), a.T, (int)a.K,
+                                                                  (int)a.N);
   return cudaGetLastError();
 }
 

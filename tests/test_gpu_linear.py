@@ -83,15 +83,18 @@ def test_weight_cast(layout):
         np.testing.assert_array_equal(s.cpu().numpy(), to_mma_layout(os_))
 
 
-def linear_case(T, K, N, seed, rows=None):
+def linear_case(T, K, N, seed, rows=None, out_offset=0):
     x = synth.make_activations(synth.WORKLOADS["llama3_8b_65536x4096"], rows=T)[:, :K] if K <= 4096 else None
     xb = np.ascontiguousarray(x)
     xc, xs, inv = oracle.mxnorm_quant(xb, 2, "mxfp8")
     wb = synth.make_random_rows(N, K, seed=seed, scale=0.03)
     wc, ws = oracle.mx_cast(wb, "mxfp8")
+    out = None
+    if out_offset:  # an output that starts out_offset elements into its allocation
+        out = torch.empty(T * N + out_offset, dtype=torch.bfloat16, device="cuda")[out_offset:].view(T, N)
     out = mx.linear_fwd(torch.from_numpy(xc).cuda(), torch.from_numpy(to_mma_layout(xs)).cuda(),
                         torch.from_numpy(inv).cuda(), torch.from_numpy(wc).cuda(),
-                        torch.from_numpy(to_mma_layout(ws)).cuda())
+                        torch.from_numpy(to_mma_layout(ws)).cuda(), out=out)
     torch.cuda.synchronize()
     got = out.float().cpu().numpy().astype(np.float64)
     rows = np.arange(T) if rows is None else np.asarray(rows)
@@ -134,6 +137,12 @@ def test_linear_many_tiles_per_pair_sampled():
     rng = np.random.default_rng(1)
     rows = np.unique(np.concatenate([np.arange(0, T, 251), np.arange(T - 4, T), rng.integers(0, T, 8)]))
     linear_case(T, 1024, 4096, seed=11, rows=rows)
+
+
+def test_linear_out_16_byte_aligned():
+    """An output only 16-byte aligned (the API's minimum) takes the 16-byte
+    store form of the epilogue."""
+    linear_case(384, 256, 512, seed=5, out_offset=8)
 
 
 def test_linear_no_device_error_flag():
