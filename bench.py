@@ -279,6 +279,43 @@ def run_gpu(args):
                                 "bytes_per_row": 2 * H + H // 2 + H // 16 + 4}
     del c4n, s4n
 
+    y_ws = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+
+    def base_step(i):
+        c, s, v = outs[i]
+        st = mx.lib().rmsnorm_mxfp8_ref_fwd(xs[i].data_ptr(), T, H, ctypes.c_float(1e-5), y_ws.data_ptr(),
+                                            c.data_ptr(), s.data_ptr(), v.data_ptr(), ctypes.c_void_p(sptr))
+        if st:
+            raise RuntimeError(mx.lib().mxnorm_last_error().decode())
+
+    perb, _ = time_launches(torch, stream, base_step, sec_steps, 5, nbuf)
+    mb = statistics.fmean(perb)
+    extra["two_pass_rmsnorm_mxfp8_baseline"] = {
+        "ms": round(mb, 5), "GB/s": gbs(baseline_bytes(T, H), mb),
+        "speedup_of_mxnorm_p2": round(mb / mean_launch, 3)}
+    del y_ws
+
+    if not args.skip_fp4:
+        # the rotated formats on the MXFP4+H16 workload's input (same distribution, seed 4)
+        w4 = synth.WORKLOADS["llama3_8b_mxfp4_h16_65536x4096"]
+        x4 = torch.from_numpy(synth.make_activations(w4).view(np.int16)).view(torch.bfloat16).to(dev)
+        c4 = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        for fmt in ("mxfp4_h16", "mxfp4_h32", "mxfp8_h16", "mxfp8_h32"):
+            fid = mx.FMT[fmt]
+
+            def fp4_step(i, fid=fid):
+                c, s, v = outs[i]
+                mx.mxnorm_quant_fwd(x4.data_ptr(), T, H, 2, fid, c4.data_ptr(), s.data_ptr(), v.data_ptr(), sptr, 0)
+
+            per4, _ = time_launches(torch, stream, fp4_step, sec_steps, 5, nbuf)
+            m = statistics.fmean(per4)
+            b4 = algorithmic_bytes(T, H, "mxfp8" if fmt.startswith("mxfp8") else "mxfp4")
+            extra[f"mxnorm_{fmt}_p2"] = {"workload": "llama3_8b_mxfp4_h16_65536x4096", "ms": round(m, 5),
+                                         "GB/s": gbs(b4, m), "frac": round(gbs(b4, m) / hbm_peak, 4)}
+        del x4, c4
+
+    # Last of the device legs: the dense GEMMs below draw the GPU into its
+    # power cap, which would depress the HBM-bound legs timed after them.
     # MXNormLinear on the tensor cores: the same rows quantised with the
     # scales in the MMA atom layout, then the block-scaled GEMM against a
     # 4096 x 4096 MXFP8 weight (a Llama-3-8B projection) with the inv_rms
@@ -357,41 +394,6 @@ def run_gpu(args):
     else:
         lin["cublaslt_mxfp8_same_inputs"] = cublas_note
     del w_codes, w_scales, xq_codes, xq_scales, xq_inv, lin_out, a8, b8
-
-    y_ws = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-
-    def base_step(i):
-        c, s, v = outs[i]
-        st = mx.lib().rmsnorm_mxfp8_ref_fwd(xs[i].data_ptr(), T, H, ctypes.c_float(1e-5), y_ws.data_ptr(),
-                                            c.data_ptr(), s.data_ptr(), v.data_ptr(), ctypes.c_void_p(sptr))
-        if st:
-            raise RuntimeError(mx.lib().mxnorm_last_error().decode())
-
-    perb, _ = time_launches(torch, stream, base_step, sec_steps, 5, nbuf)
-    mb = statistics.fmean(perb)
-    extra["two_pass_rmsnorm_mxfp8_baseline"] = {
-        "ms": round(mb, 5), "GB/s": gbs(baseline_bytes(T, H), mb),
-        "speedup_of_mxnorm_p2": round(mb / mean_launch, 3)}
-    del y_ws
-
-    if not args.skip_fp4:
-        # the rotated formats on the MXFP4+H16 workload's input (same distribution, seed 4)
-        w4 = synth.WORKLOADS["llama3_8b_mxfp4_h16_65536x4096"]
-        x4 = torch.from_numpy(synth.make_activations(w4).view(np.int16)).view(torch.bfloat16).to(dev)
-        c4 = torch.empty((T, H), dtype=torch.uint8, device=dev)
-        for fmt in ("mxfp4_h16", "mxfp4_h32", "mxfp8_h16", "mxfp8_h32"):
-            fid = mx.FMT[fmt]
-
-            def fp4_step(i, fid=fid):
-                c, s, v = outs[i]
-                mx.mxnorm_quant_fwd(x4.data_ptr(), T, H, 2, fid, c4.data_ptr(), s.data_ptr(), v.data_ptr(), sptr, 0)
-
-            per4, _ = time_launches(torch, stream, fp4_step, sec_steps, 5, nbuf)
-            m = statistics.fmean(per4)
-            b4 = algorithmic_bytes(T, H, "mxfp8" if fmt.startswith("mxfp8") else "mxfp4")
-            extra[f"mxnorm_{fmt}_p2"] = {"workload": "llama3_8b_mxfp4_h16_65536x4096", "ms": round(m, 5),
-                                         "GB/s": gbs(b4, m), "frac": round(gbs(b4, m) / hbm_peak, 4)}
-        del x4, c4
 
     # ---- e2e through the public API from pinned host buffers
     e2e = run_e2e(torch, mx, x_host, T, H, dev, args.e2e_steps)
@@ -555,6 +557,43 @@ def run_profile_case(args):
                       "GB/s": round(nbytes / (m * 1e-3) / 1e9, 1)}), flush=True)
 
 
+def run_shape_sweep(args):
+    """The MXFP8 p = 2 warp-row path across row lengths H, each on 512 MiB of
+    bf16 input: the headline workload's seeded activations (65536 x 4096)
+    viewed as rows of H, and a second buffer holding the same rows in
+    another order (two rotating buffers, so every launch streams from HBM).
+    One JSON line; not the benchmark result."""
+    import torch
+
+    import mx_scale_reusing_gb300 as mx
+    from mx_scale_reusing_gb300 import synth
+    peaks, _ = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    stream = torch.cuda.Stream()
+    xb = synth.make_activations(synth.WORKLOADS[WORKLOAD])
+    x0 = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    bases = [x0.reshape(-1), torch.roll(x0, 4099, dims=0).reshape(-1)]
+    del xb
+    res = {}
+    for H in (256, 512, 768, 1024, 2048, 4096, 8192):
+        T = bases[0].numel() // H
+        xs = [b[: T * H].view(T, H) for b in bases]
+        outs = [(torch.empty((T, H), dtype=torch.uint8, device="cuda"),
+                 torch.empty((T, H // 32), dtype=torch.uint8, device="cuda"),
+                 torch.empty((T,), dtype=torch.float32, device="cuda")) for _ in range(2)]
+
+        def fn(i):
+            mx.quant_fwd(xs[i], 2, "mxfp8", out=outs[i], stream=stream)
+        per, _ = time_launches(torch, stream, fn, args.steps, args.warmup, 2)
+        m = statistics.fmean(per)
+        g_s = algorithmic_bytes(T, H, "mxfp8") / (m * 1e-3) / 1e9
+        res[str(H)] = {"T": T, "ms": round(m, 5), "GB/s": round(g_s, 1), "frac": round(g_s / hbm_peak, 4)}
+        del xs, outs
+    print(json.dumps({"shape_sweep": True, "fmt": "mxfp8", "p": 2, "peak_GBps": hbm_peak,
+                      "launches_per_shape": args.steps, "data": f"{WORKLOAD} activations viewed as rows of H",
+                      "H": res}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -572,6 +611,8 @@ def main():
     ap.add_argument("--profile-fmt", default="mxfp8", choices=["mxfp8", "mxfp4_h16"])
     ap.add_argument("--profile-baseline", action="store_true",
                     help="profiling case: the two-pass baseline instead of MXNorm")
+    ap.add_argument("--shape-sweep", action="store_true",
+                    help="time the MXFP8 path across H = 256 .. 8192 on 512 MiB inputs (one JSON line)")
     ap.add_argument("--profile-linear", action="store_true",
                     help="profiling case: MXNormLinear's GEMM (mxnorm_linear_fwd) on the first N rows "
                          "against a 4096 x 4096 weight")
@@ -580,6 +621,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.shape_sweep:
+        run_shape_sweep(args)
     elif args.profile_rows:
         run_profile_case(args)
     else:

@@ -161,6 +161,15 @@ __device__ __forceinline__ uint8_t* scale_ptr(uint8_t* scales, int64_t row, int 
   return scales + atom * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (kb & 3);
 }
 
+// The same address split for the streaming loop: scale_row(row) +
+// (kb >> 2) * scale_quad_stride + (kb & 3), with a quad stride of 4 bytes
+// (row-major) or 512 (one atom per 4 blocks), so the per-chunk address is
+// one multiply-add and no branch.
+__device__ __forceinline__ uint8_t* scale_row(uint8_t* scales, int64_t row, int K, int tiled) {
+  if (!tiled) return scales + row * (int64_t)K;
+  return scales + (row >> 7) * (int64_t)(K >> 2) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
+}
+
 // Power mean of a row from the exponents each lane collected (ev[c] for its
 // chunks, meaningful where own[c]): m = the row's largest exponent (warp
 // max), then the fixed-point sum sum_k 2^(F + p (e_k - m)) (terms below 2^0
@@ -214,6 +223,10 @@ __device__ __forceinline__ void mx_rows_stream(const uint16_t* __restrict__ x, i
   const int64_t code_row = Tr::fp4 ? (int64_t)(Hc / 2) : (int64_t)Hc;
   if (row >= T) return;
 
+  // scale address of chunk c for this lane: scale_row(row) + loff + c * (VEC / 4) * qstride
+  const int qstride = scale_tiled ? 512 : 4;
+  const int kl = lane * VEC / kBlock;
+  const int loff = (kl >> 2) * qstride + (kl & 3);
   uint32_t buf[AHEAD][VEC / 2];
   auto issue = [&](int64_t r, int c, uint32_t (&dst)[VEC / 2]) {
     const int e0 = c * CE + lane * VEC;
@@ -230,6 +243,7 @@ __device__ __forceinline__ void mx_rows_stream(const uint16_t* __restrict__ x, i
   for (; row < T; row += rstride) {
     const int64_t next = row + rstride;
     uint8_t* cr = codes + row * code_row;
+    uint8_t* sr = scale_row(scales, row, K, scale_tiled) + loff;
     int ev[NCHUNK];
     bool own[NCHUNK];
 #pragma unroll
@@ -242,8 +256,8 @@ __device__ __forceinline__ void mx_rows_stream(const uint16_t* __restrict__ x, i
       else if (next < T) issue(next, cc - NCHUNK, buf[c % AHEAD]);
       const int e0 = c * CE + lane * VEC;
       const bool valid = EXACT || e0 < Hc;
-      ev[c] = cast_lane<FMT, VEC>(w, valid, cr + (Tr::fp4 ? e0 / 2 : e0),
-                                  scale_ptr(scales, row, e0 / kBlock, K, scale_tiled), lead);
+      static_assert(VEC % 4 == 0, "a chunk spans whole quads of blocks");
+      ev[c] = cast_lane<FMT, VEC>(w, valid, cr + (Tr::fp4 ? e0 / 2 : e0), sr + c * (VEC / 4) * qstride, lead);
       own[c] = valid && lead;
     }
     if constexpr (ESTIMATE) {

@@ -25,14 +25,17 @@ namespace warp_row {
 constexpr int kWarpsPerCta = 8;
 
 // MINB: CTAs per SM the register allocation must allow (occupancy floor).
-template <int FMT, int VEC, int NCHUNK, int AHEAD, bool EXACT, bool LOAD32, bool ESTIMATE, int MINB>
+// TILED: the scale layout (0 row-major, 1 MMA atoms) as a compile-time
+// constant; taken at run time it cost up to a fifth of the bandwidth on
+// short rows (per-row address work).
+template <int FMT, int VEC, int NCHUNK, int AHEAD, bool EXACT, bool LOAD32, bool ESTIMATE, int MINB, int TILED>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, MINB)
     mx_warp_row_kernel(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
-                       uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p, int scale_tiled) {
+                       uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p, int /*scale_tiled*/) {
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
   mx_rows_stream<FMT, VEC, NCHUNK, AHEAD, EXACT, LOAD32, ESTIMATE>(x, T, H, codes, scales, inv_rms, p,
-                                                                   warp0, nwarps, scale_tiled);
+                                                                   warp0, nwarps, TILED);
 }
 
 // Any H (a multiple of 32): batches of four chunks per row.
@@ -74,19 +77,35 @@ cudaError_t launch_kernel(Kern kern, const WarpRowArgs& a, cudaStream_t stream) 
 template <int FMT, int VEC, int NCHUNK>
 struct StreamTuning {
   static constexpr bool fp4 = FmtTraits<FMT>::fp4;
+  // Unrotated FP8 rows of 16-byte lanes: 8192- and 2048-element rows keep 4
+  // chunks in flight at 2 CTAs/SM; 1024-element rows the whole row at 3.
+  static constexpr bool plain_fp8 = !fp4 && FmtTraits<FMT>::rot == 0;
+  static constexpr bool fp8_deep = plain_fp8 && VEC == 16 && (NCHUNK == 16 || NCHUNK == 4);
+  static constexpr bool fp8_two = plain_fp8 && VEC == 16 && NCHUNK == 2;
   static constexpr int ahead = (VEC == 8) ? NCHUNK
                                : (VEC == 32) ? ((!FmtTraits<FMT>::fp4 && NCHUNK % 2 == 0) ? 2 : 1)
+                               : fp8_deep ? 4
                                : (fp4 && NCHUNK % 2 == 0) ? 2 : (NCHUNK == 2 ? 2 : 1);
   static constexpr int minb = (VEC == 32) ? 2
+                              : fp8_deep ? 2
+                              : fp8_two ? 3
                               : (VEC == 8 && NCHUNK == 1) ? 8 : (!fp4 && NCHUNK >= 8) ? 3 : 4;
 };
 
-template <int FMT, int VEC, int NCHUNK, bool LOAD32, bool ESTIMATE>
-cudaError_t launch_stream(const WarpRowArgs& a, cudaStream_t s) {
+template <int FMT, int VEC, int NCHUNK, bool LOAD32, bool ESTIMATE, int TILED>
+cudaError_t launch_stream_layout(const WarpRowArgs& a, cudaStream_t s) {
   using Tu = StreamTuning<FMT, VEC, NCHUNK>;
   if (a.H == (int64_t)NCHUNK * 32 * VEC)
-    return launch_kernel(mx_warp_row_kernel<FMT, VEC, NCHUNK, Tu::ahead, true, LOAD32, ESTIMATE, Tu::minb>, a, s);
-  return launch_kernel(mx_warp_row_kernel<FMT, VEC, NCHUNK, Tu::ahead, false, LOAD32, ESTIMATE, Tu::minb>, a, s);
+    return launch_kernel(mx_warp_row_kernel<FMT, VEC, NCHUNK, Tu::ahead, true, LOAD32, ESTIMATE, Tu::minb, TILED>, a,
+                         s);
+  return launch_kernel(mx_warp_row_kernel<FMT, VEC, NCHUNK, Tu::ahead, false, LOAD32, ESTIMATE, Tu::minb, TILED>, a,
+                       s);
+}
+
+template <int FMT, int VEC, int NCHUNK, bool LOAD32, bool ESTIMATE>
+cudaError_t launch_stream(const WarpRowArgs& a, cudaStream_t s) {
+  if (a.scale_tiled) return launch_stream_layout<FMT, VEC, NCHUNK, LOAD32, ESTIMATE, 1>(a, s);
+  return launch_stream_layout<FMT, VEC, NCHUNK, LOAD32, ESTIMATE, 0>(a, s);
 }
 
 template <int FMT, int VEC, bool LOAD32, bool ESTIMATE>
