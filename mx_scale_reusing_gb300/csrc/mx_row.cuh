@@ -267,6 +267,106 @@ __device__ __forceinline__ void mx_rows_stream(const uint16_t* __restrict__ x, i
   }
 }
 
+// finish_row over a half warp (16 lanes, one row): the same reductions with
+// shuffle offsets below 16, so the two halves of the warp finish their own
+// rows side by side.  Returns the row's inv_rms in every lane of the half.
+template <int NCHUNK>
+__device__ __forceinline__ float finish_row_half(const int (&ev)[NCHUNK], const bool (&own)[NCHUNK], int K, int p) {
+  int mloc = kExpNone;
+  bool bad = false;
+#pragma unroll
+  for (int c = 0; c < NCHUNK; ++c) {
+    if (own[c]) {
+      if (ev[c] == kExpNone) bad = true;
+      else mloc = max(mloc, ev[c]);
+    }
+  }
+  int m = mloc;
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  unsigned long long s = 0ull;
+#pragma unroll
+  for (int c = 0; c < NCHUNK; ++c) {
+    const int t = kFixedBits + p * (ev[c] - m);
+    if (own[c] && ev[c] != kExpNone && t >= 0) s += 1ull << t;
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+  const unsigned half_bad = __ballot_sync(0xFFFFFFFFu, bad) >> (threadIdx.x & 16);
+  if (half_bad & 0xFFFFu) return __uint_as_float(0x7FC00000u);
+  return pm_inv_rms(PowerMeanAcc{m, s}, K, p);
+}
+
+// Streaming loop with two rows per warp, for rows of NCHUNK chunks of
+// 16 * VEC elements (H = NCHUNK * 16 * VEC exactly): lanes 0-15 walk rows
+// row0, row0 + rstride, ... and lanes 16-31 the row after each.  Short rows
+// (H = 256 x odd) then keep 32-byte lanes and whole chunks, and the row
+// tail (power-mean reductions, root and reciprocal) serves two rows per
+// instruction.  A half whose row is past T still takes part in the
+// shuffles but stores nothing.
+template <int FMT, int VEC, int NCHUNK, int AHEAD, bool LOAD32, bool ESTIMATE>
+__device__ __forceinline__ void mx_rows_stream_half(const uint16_t* __restrict__ x, int64_t T, int H,
+                                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                    float* __restrict__ inv_rms, int p, int64_t pair_row,
+                                                    int64_t rstride, int scale_tiled) {
+  static_assert(NCHUNK % AHEAD == 0, "the ring must tile the row");
+  static_assert(VEC % 8 == 0 && kBlock / VEC <= 16, "whole quads of blocks per chunk, blocks inside a half warp");
+  using Tr = FmtTraits<FMT>;
+  constexpr int LPB = kBlock / VEC;
+  constexpr int CE = 16 * VEC;
+  constexpr int Hc = NCHUNK * CE;
+  constexpr int K = Hc / kBlock;
+  const int lane = threadIdx.x & 31;
+  const int hl = lane & 15;
+  const int64_t half = lane >> 4;
+  const bool lead = (hl % LPB) == 0;
+  const int64_t code_row = Tr::fp4 ? (int64_t)(Hc / 2) : (int64_t)Hc;
+  const int qstride = scale_tiled ? 512 : 4;
+  const int kl = hl * VEC / kBlock;
+  const int loff = (kl >> 2) * qstride + (kl & 3);
+  (void)H;
+  int64_t row = 2 * pair_row + half;
+  if (2 * pair_row >= T) return;
+
+  uint32_t buf[AHEAD][VEC / 2];
+  auto issue = [&](int64_t r, int c, uint32_t (&dst)[VEC / 2]) {
+    if (r < T) {
+      load_lane<VEC, LOAD32>(x + r * (int64_t)Hc + c * CE + hl * VEC, dst);
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC / 2; ++i) dst[i] = 0u;
+    }
+  };
+#pragma unroll
+  for (int a = 0; a < AHEAD; ++a) issue(row, a, buf[a]);
+
+  for (; row - half < T; row += 2 * rstride) {
+    const int64_t next = row + 2 * rstride;
+    const bool live = row < T;
+    uint8_t* cr = codes + row * code_row;
+    uint8_t* sr = scale_row(scales, live ? row : 0, K, scale_tiled) + loff;
+    int ev[NCHUNK];
+    bool own[NCHUNK];
+#pragma unroll
+    for (int c = 0; c < NCHUNK; ++c) {
+      uint32_t w[VEC / 2];
+#pragma unroll
+      for (int i = 0; i < VEC / 2; ++i) w[i] = buf[c % AHEAD][i];
+      const int cc = c + AHEAD;
+      if (cc < NCHUNK) issue(row, cc, buf[c % AHEAD]);
+      else issue(next, cc - NCHUNK, buf[c % AHEAD]);
+      const int e0 = c * CE + hl * VEC;
+      // a chunk spans 16 * VEC elements = VEC / 2 blocks = VEC / 8 quads of blocks
+      ev[c] = cast_lane<FMT, VEC>(w, live, cr + (Tr::fp4 ? e0 / 2 : e0), sr + c * (VEC / 8) * qstride, lead);
+      own[c] = lead;
+    }
+    if constexpr (ESTIMATE) {
+      const float inv = finish_row_half<NCHUNK>(ev, own, K, p);
+      if (hl == 0 && live) inv_rms[row] = inv;
+    }
+  }
+}
+
 // One row through a loader `load(e0, w)` (e0 = the lane's first element):
 // NCHUNK > 0 issues all of the row's loads before any arithmetic; NCHUNK ==
 // 0 handles any H in batches of four chunks with the running-maximum

@@ -183,7 +183,7 @@ def test_full_size_workloads_sampled_rows(name, fmt, ps):
 
 # --------------------------------------------------------- edge cases
 SHAPES = [(1, 32), (3, 96), (13, 800), (7, 8224), (33, 256), (11, 512), (9, 768), (41, 1024), (17, 2048), (100, 4096),
-          (5, 4128), (6, 8192)]
+          (5, 4128), (6, 8192), (7, 1280), (2, 256), (1, 768)]
 
 
 @pytest.mark.parametrize("T,H", SHAPES)
