@@ -228,6 +228,35 @@ def test_special_rows(H, fmt):
     assert (s[0] == 0).all() and i[0] == np.float32(2.0 ** 127)
 
 
+def tiny_block_rows(H, seed):
+    """Rows whose 32-element blocks sit at bf16 exponent fields from 60 down
+    to 0 (2^-67 .. subnormal), one level per block, with random mantissas
+    and signs; the last rows mix a normal value into tiny blocks.  After the
+    H16 butterfly these blocks straddle max |z| = 2^-100, where the kernel
+    switches between folding the quarter into the exponent and applying it
+    explicitly."""
+    rng = np.random.default_rng(seed)
+    K = H // 32
+    fields = np.linspace(60, 0, K).round().astype(np.int64)
+    rows = []
+    for r in range(6):
+        f = np.repeat(np.clip(fields - 2 * r, 0, 254), 32)
+        mant = rng.integers(0, 128, H)
+        sign = rng.integers(0, 2, H) << 15
+        row = (sign | (f << 7) | mant).astype(np.uint16)
+        if r >= 4:
+            row[rng.integers(0, H, 4)] = 0x3F80  # 1.0 inside some tiny blocks
+        rows.append(row)
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_tiny_blocks(fmt):
+    xb = tiny_block_rows(1024, 3)
+    for p in (1, 2):
+        assert_parity(xb, p, fmt)
+
+
 def test_empty_input_is_a_noop():
     x = torch.empty((0, 4096), dtype=torch.bfloat16, device="cuda")
     c, s, i = mx.quant_fwd(x)
