@@ -98,9 +98,9 @@ struct StreamTuning {
                                : (VEC == 32) ? ((!FmtTraits<FMT>::fp4 && NCHUNK % 2 == 0) ? 2 : 1)
                                : fp8_deep ? 4
                                : (fp4 && NCHUNK % 2 == 0) ? 2 : (NCHUNK == 2 ? 2 : 1);
-  // 64-byte lanes: 2 CTAs/SM, but the H16 rotation over FP4 at 3 (its
-  // fastest measured point, 80 registers)
-  static constexpr int minb = (VEC == 32) ? ((fp4 && FmtTraits<FMT>::rot == 16) ? 3 : 2)
+  // 64-byte lanes: FP8 at 2 CTAs/SM, FP4 (H16 and H32) at 3 (80 registers;
+  // measured 7 % and 3 % faster than 2)
+  static constexpr int minb = (VEC == 32) ? (fp4 ? 3 : 2)
                               : fp8_deep ? 2
                               : fp8_two ? 3
                               : (VEC == 8 && NCHUNK == 1) ? 8 : (!fp4 && NCHUNK >= 8) ? 3 : 4;
