@@ -84,7 +84,10 @@ def test_weight_cast(layout):
 
 
 def linear_case(T, K, N, seed, rows=None, out_offset=0):
-    x = synth.make_activations(synth.WORKLOADS["llama3_8b_65536x4096"], rows=T)[:, :K] if K <= 4096 else None
+    if K <= 4096:
+        x = synth.make_activations(synth.WORKLOADS["llama3_8b_65536x4096"], rows=T)[:, :K]
+    else:
+        x = synth.make_random_rows(T, K, seed=seed + 1, scale=2.0)
     xb = np.ascontiguousarray(x)
     xc, xs, inv = oracle.mxnorm_quant(xb, 2, "mxfp8")
     wb = synth.make_random_rows(N, K, seed=seed, scale=0.03)
@@ -137,6 +140,12 @@ def test_linear_many_tiles_per_pair_sampled():
     rng = np.random.default_rng(1)
     rows = np.unique(np.concatenate([np.arange(0, T, 251), np.arange(T - 4, T), rng.integers(0, T, 8)]))
     linear_case(T, 1024, 4096, seed=11, rows=rows)
+
+
+def test_linear_long_k():
+    """K = 8192: 64 K stages per tile, so the 6-deep stage ring and its
+    TMEM scale slots wrap many times inside one accumulation."""
+    linear_case(300, 8192, 512, seed=13)
 
 
 def test_linear_out_16_byte_aligned():
