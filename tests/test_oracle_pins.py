@@ -13,6 +13,7 @@ No GPU is used.
 """
 from fractions import Fraction
 import math
+import os
 
 import numpy as np
 import pytest
@@ -52,6 +53,59 @@ def test_e8m0_exponent_exhaustive_vs_bit_fields(oracle_mod, emax):
 def test_e8m0_exponent_fp32_range(oracle_mod):
     a = np.array([2.0 ** -149, 2.0 ** -126, 1.0, 1.9999, 2.0, 448.0, 3.0e38])
     np.testing.assert_array_equal(oracle_mod.e8m0_exponent(a, 8), [-127, -127, -8, -8, -7, 0, 119])
+
+
+# ------------------------------------------------------ spec fixtures
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "ocp_mx_v1_encodings.txt")
+
+
+def golden_rows():
+    rows = []
+    for line in open(GOLDEN):
+        line = line.split("#", 1)[0].split()
+        if line:
+            rows.append(line)
+    return rows
+
+
+def spec_value(tok: str) -> float:
+    if tok == "nan":
+        return math.nan
+    if tok == "-0":
+        return -0.0
+    return float.fromhex(tok) if "p" in tok else float(tok)
+
+
+def test_golden_ocp_encodings(oracle_mod):
+    """The oracle's E4M3 / E2M1 decodes, E8M0 scale values and shared
+    exponent against the OCP MX v1.0 tables (tests/golden)."""
+    rows = golden_rows()
+    assert len(rows) >= 30
+    for kind, a, b, *rest in rows:
+        if kind in ("e4m3", "e2m1"):
+            code, want = int(a, 16), spec_value(b)
+            got = oracle_mod.decode_e4m3(code) if kind == "e4m3" else oracle_mod.decode_e2m1(code)
+            if math.isnan(want):
+                assert math.isnan(got), (kind, a)
+            else:
+                assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), (kind, a, got)
+                if kind == "e4m3":  # and the cast maps the value back to its code
+                    assert oracle_mod.cast_e4m3([want])[0] == code, (kind, a)
+                else:
+                    assert oracle_mod.cast_e2m1([want])[0] == code, (kind, a)
+        elif kind == "e8m0":
+            code, want = int(a, 16), spec_value(b)
+            if math.isnan(want):
+                assert code == 0xFF
+            else:  # the scale a code stands for: 2^(code - 127)
+                assert math.ldexp(1.0, code - 127) == want
+                e = oracle_mod.e8m0_exponent([want * 256.0], 8)[0]  # amax = scale * 2^emax
+                assert e + 127 == code or code == 0x00, (a, e)
+        elif kind == "shared":
+            emax, amax, want = int(a), spec_value(b), int(rest[0])
+            assert oracle_mod.e8m0_exponent([amax], emax)[0] == want, (emax, b)
+        else:
+            raise AssertionError(f"unknown fixture kind {kind}")
 
 
 # ----------------------------------------------------------------- E4M3
