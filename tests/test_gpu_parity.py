@@ -158,6 +158,8 @@ def sample_rows(T, n=192, seed=0):
     ("llama3_8b_mxfp4_h16_65536x4096", "mxfp4_h16", (2,)),
     ("llama3_8b_mxfp4_h16_65536x4096", "mxfp4_h32", (2,)),
     ("llama3_8b_mxfp4_h16_65536x4096", "mxfp8_h16", (2,)),
+    ("llama3_8b_mxfp4_h16_65536x4096", "mxfp8_h32", (2,)),
+    ("llama3_8b_65536x4096", "mxfp4", (2,)),
 ])
 def test_full_size_workloads_sampled_rows(name, fmt, ps):
     """Full-size inputs in the launch configuration the benchmark times
