@@ -122,16 +122,22 @@ cudaError_t launch_stream(const WarpRowArgs& a, cudaStream_t s) {
   return launch_stream_layout<FMT, VEC, NCHUNK, LOAD32, ESTIMATE, 0>(a, s);
 }
 
-// Two rows per warp, 32-byte lanes: the whole row in flight; 3-chunk rows
-// at 2 CTAs/SM (measured 100 % of the HBM copy peak at H = 768 against
-// 88 % for one row per warp with 16-byte lanes), 1-chunk rows at 4 (96 %
-// at H = 256 against 68 %).
+// Two rows per warp, 32-byte lanes (interleaved sweeps, MXFP8 p = 2):
+//   1 chunk  (H = 256): depth 1, 4 CTAs/SM (96 % of the HBM copy peak
+//            against 68 % for one row per warp);
+//   2 chunks (H = 512): the whole row in flight, 3 CTAs/SM (3 % faster than
+//            one row per warp);
+//   3 chunks (H = 768): the whole row, 2 CTAs/SM (100 % against 88 % for
+//            one row per warp with 16-byte lanes);
+//   4 chunks (H = 1024): depth 2, 3 CTAs/SM (3 % faster);
+//   5 chunks (H = 1280): the whole row, 2 CTAs/SM.
 template <int FMT, int NCHUNK, bool ESTIMATE>
 cudaError_t launch_2row(const WarpRowArgs& a, cudaStream_t s) {
-  constexpr int MINB = NCHUNK == 1 ? 4 : 2;
+  constexpr int AHEAD = NCHUNK == 4 ? 2 : NCHUNK;
+  constexpr int MINB = NCHUNK == 1 ? 4 : (NCHUNK == 2 || NCHUNK == 4) ? 3 : 2;
   if (a.scale_tiled)
-    return launch_kernel(mx_warp_2row_kernel<FMT, 16, NCHUNK, NCHUNK, ESTIMATE, MINB, 1>, a, s, 2);
-  return launch_kernel(mx_warp_2row_kernel<FMT, 16, NCHUNK, NCHUNK, ESTIMATE, MINB, 0>, a, s, 2);
+    return launch_kernel(mx_warp_2row_kernel<FMT, 16, NCHUNK, AHEAD, ESTIMATE, MINB, 1>, a, s, 2);
+  return launch_kernel(mx_warp_2row_kernel<FMT, 16, NCHUNK, AHEAD, ESTIMATE, MINB, 0>, a, s, 2);
 }
 
 template <int FMT, int VEC, bool LOAD32, bool ESTIMATE>
@@ -168,6 +174,12 @@ cudaError_t launch_fmt(const WarpRowArgs& a, cudaStream_t s) {
         case 5: return launch_2row<FMT, 5, ESTIMATE>(a, s);
         default: break;
       }
+    }
+    // unrotated FP8 rows of 512 and 1024 elements too (measured faster than
+    // one row per warp; the other formats keep their lanes)
+    if constexpr (rot == 0 && !FmtTraits<FMT>::fp4) {
+      if (x32 && a.H == 512) return launch_2row<FMT, 2, ESTIMATE>(a, s);
+      if (x32 && a.H == 1024) return launch_2row<FMT, 4, ESTIMATE>(a, s);
     }
   }
   if constexpr (rot == 32) {
