@@ -70,6 +70,8 @@ def _load():
     lib.oracle_mxnorm_rows.restype = i32
     lib.oracle_mx_cast_rows.argtypes = [p, i64, i64, i32, p, p]
     lib.oracle_mx_cast_rows.restype = i32
+    lib.oracle_mx_cast_gain_rows.argtypes = [p, i64, i64, p, f32, p, p]
+    lib.oracle_mx_cast_gain_rows.restype = i32
     lib.oracle_rmsnorm_mxfp8_rows.argtypes = [p, i64, i64, f32, p, p, p, p]
     lib.oracle_rmsnorm_mxfp8_rows.restype = i32
     lib.oracle_cast_e4m3_array.argtypes = [p, i64, p]
@@ -158,6 +160,24 @@ def rmsnorm_mxfp8(x_bits: np.ndarray, eps: float = 1e-5):
     if lib.oracle_rmsnorm_mxfp8_rows(_ptr(x), T, H, float(eps), _ptr(y), _ptr(codes), _ptr(scales), _ptr(inv)) != 0:
         raise ValueError("oracle rejected arguments")
     return y, codes, scales, inv
+
+
+def mx_cast_gain(w_bits: np.ndarray, gamma, c: float = 1.0):
+    """MXFP8 cast (codes, row-major scales) of the gain-folded weight rows
+    w[n, j] * RN_fp32(c * gamma_j), each product rounded to fp32 ("MXNorm
+    ...", 2. Metodologia, Implementacion: gamma folded into the next layer's
+    weight)."""
+    lib = _load()
+    w = _as_bf16_bits(w_bits)
+    N, K = w.shape
+    g = np.ascontiguousarray(gamma, dtype=np.float32)
+    if g.shape != (K,):
+        raise ValueError("gamma must have K entries")
+    codes = np.empty((N, K), np.uint8)
+    scales = np.empty((N, K // BLOCK), np.uint8)
+    if lib.oracle_mx_cast_gain_rows(_ptr(w), N, K, _ptr(g), float(np.float32(c)), _ptr(codes), _ptr(scales)) != 0:
+        raise ValueError("oracle rejected arguments")
+    return codes, scales
 
 
 def mxfp8_linear(x_codes, x_scales, inv_rms, w_codes, w_scales) -> np.ndarray:

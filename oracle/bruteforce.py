@@ -160,6 +160,29 @@ def mx_block(values, signs, fmt: str):
     return e, [nearest_code(v / s, table, sb) for v, sb in zip(values, signs)]
 
 
+def mx_cast_gain_row(bits_row, gamma_bits, c_bits):
+    """Gain-folded MXFP8 cast of one bf16 weight row: v_j =
+    RN_fp32(x_j * RN_fp32(c * gamma_j)) in exact arithmetic, then the MX
+    cast; gamma_bits and c_bits are fp32 bit patterns of finite values.
+    Returns (code bytes, scale codes)."""
+    c = fp32_value(c_bits)
+    codes, scales = [], []
+    for k in range(0, len(bits_row), BLOCK):
+        vals, signs = [], []
+        for x_b, g_b in zip(bits_row[k:k + BLOCK], gamma_bits[k:k + BLOCK]):
+            g = round_to_fp32(c * fp32_value(g_b))
+            x = bf16_value(x_b)
+            v = round_to_fp32(x * g)
+            # IEEE sign of a product, zero included: the xor of the signs
+            g_neg = (g < 0) or (g == 0 and ((c_bits >> 31) ^ (g_b >> 31)))
+            vals.append(v)
+            signs.append(int((x_b >> 15) & 1) ^ int(bool(g_neg)))
+        e, cs = mx_block(vals, signs, "mxfp8")
+        scales.append(e + 127)
+        codes.extend(cs)
+    return codes, scales
+
+
 def mxnorm_row(bits_row, p: int, fmt: str):
     """MXNorm of one finite bf16 row (list of ints): (code bytes, scale
     codes, inv_rms as an exact fp32 value).

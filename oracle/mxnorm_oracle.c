@@ -383,6 +383,33 @@ int oracle_mx_cast_rows(const uint16_t *x, int64_t T, int64_t H, int fmt,
     return 0;
 }
 
+/* MX cast (MXFP8 E4M3) of the gain-folded weight of MXNormLinear ("MXNorm
+ * ...", Resumen tecnico, 2. Metodologia, "Implementacion": the norm's gain
+ * gamma, and with it the constant c, is folded into the next linear layer's
+ * weight).  Row n of W' holds w[n, j] * g_j with g_j = RN_fp32(c * gamma_j):
+ * each product is one fp32 multiplication (round to nearest even; this file
+ * is compiled without contraction), then the MX cast of those fp32 values
+ * as in oracle_mx_cast_rows.  w: bf16 bits [N, K]; gamma: fp32 [K]. */
+int oracle_mx_cast_gain_rows(const uint16_t *w, int64_t N, int64_t K, const float *gamma, float c,
+                             uint8_t *codes, uint8_t *scales)
+{
+    if (check_args(N, K, OR_FMT_MXFP8_E4M3)) return 1;
+    const int64_t KB = K / OR_BLOCK;
+    double v[OR_BLOCK];
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            for (int j = 0; j < OR_BLOCK; ++j) {
+                const int64_t idx = kb * OR_BLOCK + j;
+                const float g = c * gamma[idx];
+                const float y = bf16_bits_to_float(w[n * K + idx]) * g;
+                v[j] = (double)y;
+            }
+            (void)cast_block(v, OR_FMT_MXFP8_E4M3, scales + n * KB + kb, codes + n * K, kb);
+        }
+    }
+    return 0;
+}
+
 /* --------------------------------------------------------------- MXNorm */
 
 /* MXNorm forward of T rows: the MX cast of each row plus

@@ -633,3 +633,47 @@ def test_linear_identity_weight(oracle_mod):
     got = oracle_mod.mxfp8_linear(xc, xs, inv, wc, ws)
     xv = _e4m3_values(xc) * np.repeat(np.exp2(xs.astype(np.float64) - 127), 32, axis=1)
     np.testing.assert_array_equal(got, inv.astype(np.float64)[:, None] * xv)
+
+
+# ------------------------------------------------ gain-folded weight cast
+def test_gain_cast_unit_gain_is_the_plain_cast(oracle_mod):
+    from mx_scale_reusing_gb300 import synth
+    w = synth.make_random_rows(16, 512, seed=21, scale=3.0)
+    c1, s1 = oracle_mod.mx_cast_gain(w, np.ones(512, np.float32), 1.0)
+    c0, s0 = oracle_mod.mx_cast(w, "mxfp8")
+    np.testing.assert_array_equal(c1, c0)
+    np.testing.assert_array_equal(s1, s0)
+
+
+def test_gain_cast_power_of_two_shifts_the_scales(oracle_mod):
+    """gamma = 2^j everywhere (c = 1): every product is exact, so the codes
+    are the plain cast's and each scale code moves by j (normal-range
+    blocks, away from the E8M0 clamps)."""
+    from mx_scale_reusing_gb300 import synth
+    w = synth.make_random_rows(16, 256, seed=22, scale=1.0)
+    for j in (-5, 3):
+        c1, s1 = oracle_mod.mx_cast_gain(w, np.full(256, 2.0 ** j, np.float32), 1.0)
+        c0, s0 = oracle_mod.mx_cast(w, "mxfp8")
+        np.testing.assert_array_equal(c1, c0)
+        np.testing.assert_array_equal(s1.astype(int), s0.astype(int) + j)
+
+
+def test_gain_cast_vs_bruteforce(oracle_mod):
+    """Random fp32 gains (incl. +-0 and negatives) and c = 1.37: the C
+    oracle equals the exact-fraction implementation."""
+    from oracle import bruteforce as bf
+    from mx_scale_reusing_gb300 import synth
+    rng = np.random.default_rng(23)
+    K = 96
+    w = synth.make_random_rows(4, K, seed=24, scale=2.0)
+    gamma = (np.exp(rng.normal(0, 0.7, K)) * rng.choice([-1.0, 1.0], K)).astype(np.float32)
+    gamma[[3, 40]] = [0.0, -0.0]
+    gamma[7] = np.float32(3.0e-39)  # subnormal gain
+    c = np.float32(1.37)
+    oc, os_ = oracle_mod.mx_cast_gain(w, gamma, float(c))
+    gb = gamma.view(np.uint32).tolist()
+    cb = int(np.array([c], np.float32).view(np.uint32)[0])
+    for n in range(w.shape[0]):
+        codes, scales = bf.mx_cast_gain_row([int(b) for b in w[n]], gb, cb)
+        assert oc[n].tolist() == codes, n
+        assert os_[n].tolist() == scales, n
