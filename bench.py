@@ -314,6 +314,31 @@ def run_gpu(args):
                                          "GB/s": gbs(b4, m), "frac": round(gbs(b4, m) / hbm_peak, 4)}
         del x4, c4
 
+    # MXNormLinear's weight side: the gain-folded MXFP8 cast of a Llama-3-8B
+    # fused gate/up weight (28672 x 4096 bf16, 235 MB: larger than L2), scales
+    # in the MMA layout.  Bytes per row: 2K read + K codes + K/32 scales (the
+    # K gains stay in L1/L2).
+    Ng = 28672
+    gg = torch.Generator(device=dev).manual_seed(9)
+    wg = (torch.randn((Ng, H), device=dev, generator=gg) * 0.02).to(torch.bfloat16)
+    gamma = (1.0 + 0.1 * torch.randn((H,), device=dev, generator=gg)).float()
+    gc = torch.empty((Ng, H), dtype=torch.uint8, device=dev)
+    gs = torch.empty((mx.mma_scale_bytes(Ng, H),), dtype=torch.uint8, device=dev)
+
+    def gain_step(i):
+        st = mx.lib().mx_cast_gain_fwd(wg.data_ptr(), Ng, H, gamma.data_ptr(), ctypes.c_float(1.0), gc.data_ptr(),
+                                       gs.data_ptr(), 1, ctypes.c_void_p(sptr))
+        if st:
+            raise RuntimeError(mx.lib().mxnorm_last_error().decode())
+
+    perg, _ = time_launches(torch, stream, gain_step, sec_steps, 5, nbuf)
+    m = statistics.fmean(perg)
+    bg = Ng * (3 * H + H // 32)
+    extra["mx_cast_gain_llama3_8b_gate_up_28672x4096"] = {
+        "ms": round(m, 5), "GB/s": gbs(bg, m), "frac": round(gbs(bg, m) / hbm_peak, 4),
+        "bytes_per_row": 3 * H + H // 32}
+    del wg, gc, gs
+
     # Last of the device legs: the dense GEMMs below draw the GPU into its
     # power cap, which would depress the HBM-bound legs timed after them.
     # MXNormLinear on the tensor cores: the same rows quantised with the
@@ -323,8 +348,8 @@ def run_gpu(args):
     Nw = 4096
     gw = torch.Generator(device=dev).manual_seed(7)
     wt = (torch.randn((Nw, H), device=dev, generator=gw) * 0.02).to(torch.bfloat16)
-    w_codes, w_scales = mx.mx_cast(wt, "mma")
-    del wt
+    w_codes, w_scales = mx.mx_cast_gain(wt, gamma, 1.0, "mma")
+    del wt, gamma
     xq_codes = torch.empty((T, H), dtype=torch.uint8, device=dev)
     xq_scales = torch.empty((mx.mma_scale_bytes(T, H),), dtype=torch.uint8, device=dev)
     xq_inv = torch.empty((T,), dtype=torch.float32, device=dev)

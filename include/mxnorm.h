@@ -142,6 +142,25 @@ int mxnorm_quant_fwd_layout(const void* x, int64_t T, int64_t H, int p, int fmt,
 int mx_cast_fwd(const void* x, int64_t T, int64_t H, int fmt, void* codes, uint8_t* scales, int scale_layout,
                 void* stream);
 
+/* MXFP8 cast of MXNormLinear's gain-folded weight in one pass ("MXNorm ...",
+ * Resumen tecnico, 2. Metodologia, "Implementacion": the norm's gain, with
+ * the estimator constant c, moves into the next linear layer's weight).
+ * w: bf16 [N, K] device, row n = the weights of output feature n (W^T of
+ * y = x W), 16-byte aligned.  gamma: fp32 [K] device, 16-byte aligned.
+ * Element (n, k) of the cast input is w[n, k] * g_k with
+ * g_k = RN_fp32(c * gamma_k), each product rounded to fp32 (IEEE
+ * round-to-nearest-even, subnormals kept); then each 32-element block gets
+ * its E8M0 scale and saturating RNE E4M3 codes exactly as mx_cast_fwd.  A
+ * block holding Inf/NaN after the product gets scale 0xFF and codes 0x7F.
+ * codes: E4M3 [N, K] device, 16-byte aligned; scales: scale_layout
+ * (MXNORM_SCALE_MMA gives the w_scales of mxnorm_linear_fwd; needs
+ * K % 128 == 0).  Preconditions: N >= 0, 0 < K <= MXNORM_MAX_H,
+ * K % 32 == 0, c finite.  Errors: INVALID_ARG / MISALIGNED / UNSUPPORTED,
+ * checked before any launch; N == 0 returns OK with no launch.  The call
+ * owns no memory and is asynchronous on stream (cudaStream_t or NULL). */
+int mx_cast_gain_fwd(const void* w, int64_t N, int64_t K, const float* gamma, float c, void* codes,
+                     uint8_t* scales, int scale_layout, void* stream);
+
 /* Consumer side of MXNormLinear ("MXNorm ...", Resumen tecnico, 2.
  * Metodologia, "Implementacion": the gain is folded into the next linear
  * layer's weight): an MXFP8 block-scaled GEMM on the tensor cores whose

@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
     L.mxnorm_quant_fwd_layout.restype = i32
     L.mx_cast_fwd.argtypes = [vp, i64, i64, i32, vp, vp, i32, vp]
     L.mx_cast_fwd.restype = i32
+    L.mx_cast_gain_fwd.argtypes = [vp, i64, i64, vp, ctypes.c_float, vp, vp, i32, vp]
+    L.mx_cast_gain_fwd.restype = i32
     L.mxnorm_linear_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]
     L.mxnorm_linear_fwd.restype = i32
     L.mxnorm_bwd_ste.restype = i32
@@ -238,6 +240,24 @@ def mx_cast(x, layout: str = "row_major", stream=None):
     scales = _scale_buffer(T, H, layout, x.device)
     _check(lib().mx_cast_fwd(x.data_ptr(), T, H, 0, codes.data_ptr(), scales.data_ptr(), SCALE_LAYOUT[layout],
                              _stream_ptr(x.device, stream)))
+    return codes, scales
+
+
+def mx_cast_gain(w, gamma, c: float = 1.0, layout: str = "mma", stream=None):
+    """MXFP8 cast of MXNormLinear's gain-folded weight: rows of
+    w[n, k] * RN_fp32(c * gamma[k]), each product rounded to fp32.
+    w: contiguous bf16 CUDA tensor [N, K] (one row per output feature);
+    gamma: contiguous float32 CUDA tensor [K].  Returns (codes, scales)."""
+    import torch
+    if not (w.is_cuda and w.dtype == torch.bfloat16 and w.is_contiguous() and w.dim() == 2):
+        raise ValueError("w must be a contiguous 2-D bfloat16 CUDA tensor")
+    N, K = w.shape
+    if not (gamma.is_cuda and gamma.dtype == torch.float32 and gamma.is_contiguous() and gamma.shape == (K,)):
+        raise ValueError("gamma must be a contiguous float32 CUDA tensor of K entries")
+    codes = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    scales = _scale_buffer(N, K, layout, w.device)
+    _check(lib().mx_cast_gain_fwd(w.data_ptr(), N, K, gamma.data_ptr(), float(c), codes.data_ptr(),
+                                  scales.data_ptr(), SCALE_LAYOUT[layout], _stream_ptr(w.device, stream)))
     return codes, scales
 
 

@@ -20,7 +20,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmxnorm.so")
 SOURCES = ["capi.cu", "mxnorm_warp.cu", "mxnorm_warp_fp8.cu", "mxnorm_warp_fp4.cu", "mxnorm_tiled.cu",
            "rmsnorm_ref.cu", "rmsnorm_static_ws.cu", "mxnorm_bwd.cu",
-           "mxnorm_nvfp4.cu", "mxnorm_linear.cu"]
+           "mxnorm_nvfp4.cu", "mxnorm_linear.cu", "mx_cast_gain.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-I" + INCLUDE, "-I" + CSRC, "-Xptxas", "-v", "--expt-relaxed-constexpr"]

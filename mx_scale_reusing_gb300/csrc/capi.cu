@@ -1,6 +1,7 @@
 // capi.cu -- the extern "C" boundary of libmxnorm: argument validation,
 // variant selection and launches.  Declarations and the full contract are
 // in include/mxnorm.h.
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <map>
@@ -148,6 +149,29 @@ int mx_cast_fwd(const void* x, int64_t T, int64_t H, int fmt, void* codes, uint8
   a.scale_tiled = scale_layout == MXNORM_SCALE_MMA;
   cudaError_t err = launch_mx_cast_warp_row(a, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "mx_cast_fwd launch");
+  return MXNORM_OK;
+}
+
+int mx_cast_gain_fwd(const void* w, int64_t N, int64_t K, const float* gamma, float c, void* codes,
+                     uint8_t* scales, int scale_layout, void* stream) {
+  g_last_error.clear();
+  if (scale_layout != MXNORM_SCALE_ROW_MAJOR && scale_layout != MXNORM_SCALE_MMA)
+    return fail(MXNORM_ERR_INVALID_ARG, "unknown scale_layout %d", scale_layout);
+  if (N < 0) return fail(MXNORM_ERR_INVALID_ARG, "N = %lld < 0", (long long)N);
+  if (K <= 0 || K % kBlock != 0)
+    return fail(MXNORM_ERR_INVALID_ARG, "K = %lld is not a positive multiple of 32", (long long)K);
+  if (K > MXNORM_MAX_H)
+    return fail(MXNORM_ERR_UNSUPPORTED, "K = %lld exceeds MXNORM_MAX_H = %d", (long long)K, MXNORM_MAX_H);
+  if (scale_layout == MXNORM_SCALE_MMA && K % 128 != 0)
+    return fail(MXNORM_ERR_INVALID_ARG, "the MMA scale layout needs K %% 128 == 0 (K = %lld)", (long long)K);
+  if (!std::isfinite(c)) return fail(MXNORM_ERR_INVALID_ARG, "c is not finite");
+  if (N == 0) return MXNORM_OK;
+  if (!w || !gamma || !codes || !scales) return fail(MXNORM_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(w, 16) || !aligned(gamma, 16) || !aligned(codes, 16))
+    return fail(MXNORM_ERR_MISALIGNED, "w, gamma and codes need 16-byte alignment");
+  GainCastArgs a{w, N, K, gamma, c, codes, scales, scale_layout == MXNORM_SCALE_MMA};
+  cudaError_t err = launch_mx_cast_gain(a, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "mx_cast_gain_fwd launch");
   return MXNORM_OK;
 }
 

@@ -60,6 +60,17 @@ struct LinearArgs {
   void* out;                 // bf16 [T, N]
 };
 
+struct GainCastArgs {
+  const void* w;        // bf16 [N, K], one row per output feature
+  int64_t N;
+  int64_t K;            // % 32 == 0 (% 128 for the MMA layout)
+  const float* gamma;   // f32 [K], 16-byte aligned
+  float c;              // estimator constant, folded with gamma
+  void* codes;          // E4M3 [N, K]
+  uint8_t* scales;      // E8M0, row-major [N, K/32] or MMA atoms
+  int scale_tiled;      // 1: MMA atom layout
+};
+
 struct TiledArgs {
   WarpRowArgs base;
   unsigned int* error_flag;  // device word set when a bounded wait gives up
@@ -78,6 +89,7 @@ bool tiled_supported(int64_t H, int fmt);
 cudaError_t launch_mxnorm_bwd_ste(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_nvfp4(const Nvfp4Args& a, cudaStream_t s);
 cudaError_t launch_mxfp8_linear(const LinearArgs& a, cudaStream_t s);
+cudaError_t launch_mx_cast_gain(const GainCastArgs& a, cudaStream_t s);
 cudaError_t read_linear_error_word(uint32_t* out, bool clear);
 cudaError_t launch_absmax_bf16(const void* x, int64_t n, float* amax, cudaStream_t s);
 

@@ -115,6 +115,20 @@ def test_linear_and_layout_validation(L):
     assert L.mx_cast_fwd(FAKE, 8, 96, 0, FAKE, FAKE, 1, None) == 1
 
 
+def test_gain_cast_validation(L):
+    g = L.mx_cast_gain_fwd
+    assert g(FAKE, 0, 128, FAKE, 1.0, FAKE, FAKE, 1, None) == 0      # no rows: no launch
+    assert g(FAKE, -1, 128, FAKE, 1.0, FAKE, FAKE, 0, None) == 1
+    assert g(FAKE, 8, 48, FAKE, 1.0, FAKE, FAKE, 0, None) == 1       # K % 32
+    assert g(FAKE, 8, 96, FAKE, 1.0, FAKE, FAKE, 1, None) == 1       # MMA layout needs K % 128
+    assert g(FAKE, 8, 128, FAKE, 1.0, FAKE, FAKE, 5, None) == 1      # unknown layout
+    assert g(FAKE, 8, 128, FAKE, float("inf"), FAKE, FAKE, 0, None) == 1
+    assert g(FAKE, 8, 128, None, 1.0, FAKE, FAKE, 0, None) == 1
+    assert g(FAKE, 8, 128, FAKE + 4, 1.0, FAKE, FAKE, 0, None) == 3  # gamma alignment
+    assert g(FAKE, 8, 128, FAKE, 1.0, FAKE + 8, FAKE, 0, None) == 3  # codes alignment
+    assert g(FAKE, 8, (1 << 20) + 32, FAKE, 1.0, FAKE, FAKE, 0, None) == 2
+
+
 def test_python_binding_raises_on_status(L):
     with pytest.raises(mx.MXNormError) as ei:
         mx.mxnorm_quant_fwd(FAKE, 8, 48, 2, 0, FAKE, FAKE, FAKE)

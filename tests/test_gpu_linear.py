@@ -157,3 +157,108 @@ def test_linear_out_16_byte_aligned():
 def test_linear_no_device_error_flag():
     linear_case(256, 512, 256, seed=1)
     assert mx.device_errors() == 0
+
+
+# ------------------------------------------------ gain-folded weight cast
+def gains(K, seed):
+    """Norm gains around 1 with both signs, exact zeros of both signs and a
+    subnormal, as float32."""
+    rng = np.random.default_rng(seed)
+    g = (np.exp(rng.normal(0.0, 0.6, K)) * rng.choice([-1.0, 1.0], K, p=[0.1, 0.9])).astype(np.float32)
+    g[[0, K // 2]] = [0.0, -0.0]
+    g[K - 1] = np.float32(2.0e-39)
+    return g
+
+
+def check_gain_cast(wb, g, c, layout, w_dev=None, rows=None):
+    w = dev(wb) if w_dev is None else w_dev
+    codes, scales = mx.mx_cast_gain(w, torch.from_numpy(g).cuda(), c, layout)
+    torch.cuda.synchronize()
+    N, K = wb.shape
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    oc, os_ = oracle.mx_cast_gain(np.ascontiguousarray(wb[rows]), g, c)
+    got_c = codes.cpu().numpy()
+    np.testing.assert_array_equal(got_c[rows], oc)
+    got_s = scales.cpu().numpy()
+    if layout == "row_major":
+        np.testing.assert_array_equal(got_s[rows], os_)
+    else:
+        full = np.zeros((N, K // 32), np.uint8)
+        full[rows] = os_
+        mask = to_mma_layout(np.isin(np.arange(N), rows)[:, None].repeat(K // 32, 1).astype(np.uint8)) == 1
+        np.testing.assert_array_equal(got_s[mask], to_mma_layout(full)[mask])
+
+
+@pytest.mark.parametrize("layout", ["row_major", "mma"])
+@pytest.mark.parametrize("N,K", [(512, 768), (77, 4096), (300, 1152), (1, 128), (1029, 2560)])
+def test_gain_cast_parity(N, K, layout):
+    """Strips of 512 columns with a ragged last strip (768, 1152, 2560),
+    row counts off the 8-warp and 128-row tiles, c != 1."""
+    wb = synth.make_random_rows(N, K, seed=N + K, scale=0.03)
+    check_gain_cast(wb, gains(K, N), 1.7, layout)
+
+
+def test_gain_cast_short_rows_row_major():
+    """K = 32 and 96: one strip, most lanes idle."""
+    for K in (32, 96):
+        wb = synth.make_random_rows(40, K, seed=K, scale=1.0)
+        check_gain_cast(wb, gains(K, K), 0.75, "row_major")
+
+
+def test_gain_cast_special_values():
+    """Inf/NaN weights, gains whose product with c overflows (Inf, and NaN
+    where the weight is 0), subnormal products, blocks of zeros."""
+    N, K = 64, 512
+    wb = synth.make_random_rows(N, K, seed=3, scale=1.0)
+    wb[1, 5] = 0x7F80          # +Inf
+    wb[2, 40] = 0x7FC1         # NaN
+    wb[3, :32] = 0             # zero block
+    wb[4, 64:96] = 0x0001      # bf16 subnormals
+    wb[5, 300] = 0             # zero times an infinite gain -> NaN
+    g = gains(K, 4)
+    g[300] = np.float32(3.0e38)  # c * g overflows to Inf
+    g[100:132] = np.float32(1.0e-30)  # products far below the fp32 normal range
+    check_gain_cast(wb, g, 1.7, "row_major")
+    check_gain_cast(wb, g, 1.7, "mma")
+
+
+def test_gain_cast_16_byte_aligned_weight():
+    """A weight only 16-byte aligned takes the 16-byte load form."""
+    N, K = 96, 1024
+    wb = synth.make_random_rows(N, K, seed=8, scale=0.05)
+    buf = torch.empty(N * K + 8, dtype=torch.bfloat16, device="cuda")
+    w = buf[8:].view(N, K)
+    w.copy_(dev(wb))
+    assert w.data_ptr() % 32 == 16
+    check_gain_cast(wb, gains(K, 8), 1.0, "mma", w_dev=w)
+
+
+def test_gain_cast_llama3_8b_gate_up_sampled():
+    """The Llama-3-8B fused gate/up weight (28672 x 4096) in the MMA layout,
+    the oracle on sampled rows (both ends and random rows of many strips)."""
+    N, K = 28672, 4096
+    wb = synth.make_random_rows(N, K, seed=12, scale=0.02)
+    rng = np.random.default_rng(12)
+    rows = np.unique(np.concatenate([np.arange(4), np.arange(N - 4, N), rng.integers(0, N, 56)]))
+    check_gain_cast(wb, gains(K, 12), 1.0, "mma", rows=rows)
+
+
+def test_linear_with_gain_folded_weight():
+    """MXNormLinear end to end: activations through the fused pass (MMA
+    scales), the weight through the gain-folded cast, the GEMM; against the
+    oracle's chain (gain cast, then the fp64 GEMM)."""
+    T, K, N = 300, 1024, 512
+    xb = synth.make_random_rows(T, K, seed=21, scale=2.0)
+    wb = synth.make_random_rows(N, K, seed=22, scale=0.03)
+    g = gains(K, 23)
+    xc, xs, inv = mx.quant_fwd_mma(dev(xb))
+    wc, ws = mx.mx_cast_gain(dev(wb), torch.from_numpy(g).cuda(), 1.3, "mma")
+    out = mx.linear_fwd(xc, xs, inv, wc, ws)
+    torch.cuda.synchronize()
+    oxc, oxs, oxi = oracle.mxnorm_quant(xb, 2, "mxfp8")
+    owc, ows = oracle.mx_cast_gain(wb, g, 1.3)
+    np.testing.assert_array_equal(wc.cpu().numpy(), owc)
+    want = oracle.mxfp8_linear(oxc, oxs, oxi, owc, ows)
+    got = out.float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - want)
+    assert (err <= 2.0 ** -7 * np.abs(want) + 2.0 ** -12 * np.abs(want).max()).all()
