@@ -331,12 +331,24 @@ def run_gpu(args):
         if st:
             raise RuntimeError(mx.lib().mxnorm_last_error().decode())
 
-    perg, _ = time_launches(torch, stream, gain_step, sec_steps, 5, nbuf)
-    m = statistics.fmean(perg)
+    # Yardstick at the same size: the plain MXFP8 cast (the activation
+    # pass's streaming kernel without the estimator) of the same weight.
+    def plain_step(i):
+        st = mx.lib().mx_cast_fwd(wg.data_ptr(), Ng, H, 0, gc.data_ptr(), gs.data_ptr(), 1, ctypes.c_void_p(sptr))
+        if st:
+            raise RuntimeError(mx.lib().mxnorm_last_error().decode())
+
+    perg, perp = [], []
+    for _ in range(2):  # alternating blocks
+        perg += time_launches(torch, stream, gain_step, sec_steps // 2, 5, nbuf)[0]
+        perp += time_launches(torch, stream, plain_step, sec_steps // 2, 5, nbuf)[0]
+    m, mp = statistics.fmean(perg), statistics.fmean(perp)
     bg = Ng * (3 * H + H // 32)
     extra["mx_cast_gain_llama3_8b_gate_up_28672x4096"] = {
         "ms": round(m, 5), "GB/s": gbs(bg, m), "frac": round(gbs(bg, m) / hbm_peak, 4),
-        "bytes_per_row": 3 * H + H // 32}
+        "bytes_per_row": 3 * H + H // 32,
+        "plain_mx_cast_same_weight": {"ms": round(mp, 5), "GB/s": gbs(bg, mp),
+                                      "frac": round(gbs(bg, mp) / hbm_peak, 4)}}
     del wg, gc, gs
 
     # Last of the device legs: the dense GEMMs below draw the GPU into its
@@ -568,6 +580,28 @@ def run_profile_case(args):
     T, H = args.profile_rows, w.H
     x = torch.from_numpy(synth.make_activations(w, rows=T).view(np.int16)).view(torch.bfloat16).cuda()
     stream = torch.cuda.Stream()
+    if args.profile_gain:
+        # the gain-folded weight cast on the first N rows of a 4096-column
+        # weight (the Llama-3-8B gate/up weight is 28672 rows), MMA scales
+        Ng = T
+        gg = torch.Generator(device="cuda").manual_seed(9)
+        wg = (torch.randn((Ng, H), device="cuda", generator=gg) * 0.02).to(torch.bfloat16)
+        gamma = (1.0 + 0.1 * torch.randn((H,), device="cuda", generator=gg)).float()
+        gc = torch.empty((Ng, H), dtype=torch.uint8, device="cuda")
+        gs = torch.empty((mx.mma_scale_bytes(Ng, H),), dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+
+        def fn_gain(i):
+            st = mx.lib().mx_cast_gain_fwd(wg.data_ptr(), Ng, H, gamma.data_ptr(), ctypes.c_float(1.0),
+                                           gc.data_ptr(), gs.data_ptr(), 1, ctypes.c_void_p(stream.cuda_stream))
+            if st:
+                raise RuntimeError(mx.lib().mxnorm_last_error().decode())
+        per, region = time_launches(torch, stream, fn_gain, args.steps, args.warmup, 1)
+        m = statistics.fmean(per)
+        print(json.dumps({"profile_only": True, "kernel": "mx_cast_gain_fwd", "N": Ng, "K": H,
+                          "mean_launch_ms": round(m, 6),
+                          "GB/s": round(Ng * (3 * H + H // 32) / (m * 1e-3) / 1e9, 1)}), flush=True)
+        return
     if args.profile_linear:
         # MXNormLinear's GEMM: the rows quantised with MMA-layout scales
         # against a 4096 x 4096 MXFP8 weight (a Llama-3-8B projection)
@@ -668,6 +702,9 @@ def main():
     ap.add_argument("--profile-linear", action="store_true",
                     help="profiling case: MXNormLinear's GEMM (mxnorm_linear_fwd) on the first N rows "
                          "against a 4096 x 4096 weight")
+    ap.add_argument("--profile-gain", action="store_true",
+                    help="profiling case: the gain-folded MXFP8 weight cast (mx_cast_gain_fwd) of an "
+                         "N x 4096 weight")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
