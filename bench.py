@@ -295,6 +295,43 @@ def run_gpu(args):
         "speedup_of_mxnorm_p2": round(mb / mean_launch, 3)}
     del y_ws
 
+    # The Llama-3-1B-shaped workload (32768 x 2048, 128 MiB of bf16: about
+    # the size of L2), MXNorm beside the two-pass baseline.  Four input
+    # buffers rotate, so a buffer was last read three launches (384 MiB of
+    # input) earlier and streams from HBM again.
+    w1 = synth.WORKLOADS["llama3_1b_32768x2048"]
+    T1, H1 = w1.T, w1.H
+    x1h = torch.from_numpy(synth.make_activations(w1).view(np.int16)).view(torch.bfloat16)
+    nb1 = 4
+    x1 = [x1h.to(dev) for _ in range(nb1)]
+    c1 = torch.empty((T1, H1), dtype=torch.uint8, device=dev)
+    s1 = torch.empty((T1, H1 // 32), dtype=torch.uint8, device=dev)
+    i1 = torch.empty((T1,), dtype=torch.float32, device=dev)
+    y1 = torch.empty((T1, H1), dtype=torch.bfloat16, device=dev)
+
+    def mx1_step(i):
+        mx.mxnorm_quant_fwd(x1[i].data_ptr(), T1, H1, 2, 0, c1.data_ptr(), s1.data_ptr(), i1.data_ptr(), sptr, 0)
+
+    def base1_step(i):
+        st = mx.lib().rmsnorm_mxfp8_ref_fwd(x1[i].data_ptr(), T1, H1, ctypes.c_float(1e-5), y1.data_ptr(),
+                                            c1.data_ptr(), s1.data_ptr(), i1.data_ptr(), ctypes.c_void_p(sptr))
+        if st:
+            raise RuntimeError(mx.lib().mxnorm_last_error().decode())
+
+    pm1, pb1 = [], []
+    for _ in range(2):  # alternating blocks
+        pm1 += time_launches(torch, stream, mx1_step, sec_steps // 2, 5, nb1)[0]
+        pb1 += time_launches(torch, stream, base1_step, sec_steps // 2, 5, nb1)[0]
+    m1, b1 = statistics.fmean(pm1), statistics.fmean(pb1)
+    a1 = algorithmic_bytes(T1, H1, "mxfp8")
+    extra["llama3_1b_32768x2048"] = {
+        "mxnorm_mxfp8_p2": {"ms": round(m1, 5), "GB/s": gbs(a1, m1), "frac": round(gbs(a1, m1) / hbm_peak, 4),
+                            "tokens_per_s": round(T1 / (m1 * 1e-3), 1)},
+        "two_pass_rmsnorm_mxfp8_baseline": {"ms": round(b1, 5), "GB/s": gbs(baseline_bytes(T1, H1), b1),
+                                            "speedup_of_mxnorm_p2": round(b1 / m1, 3)},
+        "l2": "4 rotating 128 MiB input buffers"}
+    del x1, c1, s1, i1, y1
+
     if not args.skip_fp4:
         # the rotated formats on the MXFP4+H16 workload's input (same distribution, seed 4)
         w4 = synth.WORKLOADS["llama3_8b_mxfp4_h16_65536x4096"]
@@ -459,7 +496,8 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(achieved / hbm_peak, 4), "traffic": profiled_traffic(),
                          "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": abytes,
-                         "mean_launch_ms": round(mean_launch, 6)},
+                         "mean_launch_ms": round(mean_launch, 6),
+                         "median_launch_ms": round(statistics.median(per), 6)},
             "clocks": sampler.summary(),
             "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
