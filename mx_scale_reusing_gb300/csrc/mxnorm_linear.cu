@@ -9,8 +9,9 @@
 // with x^ the MXFP8 codes and E8M0 block scales of the row (mxnorm_quant_fwd
 // with the MMA scale layout), rho~ = inv_rms, and w'^ the MXFP8 cast of
 // W' = diag(c gamma) W, i.e. one row per output feature, quantised along K
-// (mx_cast_fwd).  The row scale commutes with the matmul, so it is applied
-// once per output element in the epilogue.
+// (mx_cast_gain_fwd folds c gamma in and casts in one pass; mx_cast_fwd casts
+// a weight that already holds them).  The row scale commutes with the
+// matmul, so it is applied once per output element in the epilogue.
 //
 // Tiling: 256 x 256 output tiles, each computed by a pair of CTAs on the two
 // SMs of a TPC (a cluster of 2): tcgen05.mma with cta_group::2, M = 256
@@ -19,29 +20,30 @@
 // one half (128 rows) of the tile's 256 w rows, K 128 bytes at a time
 // through a 6-deep shared-memory ring; the pair's tensor cores read both w
 // halves, so every w byte crosses L2 -> SM once per pair rather than once per
-// CTA.  Persistent pairs, warp-specialised (224 threads per CTA):
+// CTA.  Persistent pairs, warp-specialised (11 warps, 352 threads per CTA):
 //   warp 0 lane 0  TMA producer (both CTAs): 2-D tiled loads of the CTA's x
 //                  rows and w half (128-byte swizzle) and of the 512-byte
 //                  scale atoms (its own x atom, both w atoms), all completing
 //                  on the leader's stage "full" mbarrier (cta_group::2 form),
 //                  which expects both CTAs' bytes;
-//   warp 6 lane 0  leader CTA: scale-factor copier.  Per stage it waits for
+//   warp 1 lane 0  leader CTA: MMA issuer.  Per stage it waits for
+//                  "sf_full", issues four tcgen05.mma and commits to the
+//                  "empty" mbarriers of both CTAs (multicast); after a tile's
+//                  last stage it commits to both CTAs' "acc_full";
+//   warp 2 lane 0  leader CTA: scale-factor copier.  Per stage it waits for
 //                  "full", copies the atoms into both CTAs' TMEM (tcgen05.cp,
 //                  cta_group::2: each CTA's shared memory into its own TMEM)
 //                  and commits to "sf_full".  Copies issued by the MMA thread
 //                  itself would wait between its stages; from a thread of
 //                  their own they overlap the MMAs in flight;
-//   warp 1 lane 0  leader CTA: MMA issuer.  Per stage it waits for
-//                  "sf_full", issues four tcgen05.mma and commits to the
-//                  "empty" mbarriers of both CTAs (multicast); after a tile's
-//                  last stage it commits to both CTAs' "acc_full";
-//   warps 2-5      epilogue (both CTAs): tcgen05.ld of the CTA's fp32
-//                  accumulators (each warp its TMEM lane quadrant = 32 rows),
-//                  times rho~[row], rounded to packed bf16 in registers; an
-//                  arrival on the leader's "acc_empty" (8 per tile) frees
-//                  TMEM for the next tile's MMAs, and the rows leave through
-//                  per-warp 4 KiB swizzled staging buffers as TMA tensor
-//                  stores of 32 x 64 bf16 boxes.
+//   warps 3-10     epilogue (both CTAs), two per TMEM lane quadrant (32 rows)
+//                  with 128 columns each: tcgen05.ld of the fp32
+//                  accumulators in two 64-column steps, times rho~[row],
+//                  rounded to packed bf16 in registers; after the second
+//                  load an arrival on the leader's "acc_empty" (16 per tile)
+//                  frees TMEM for the next tile's MMAs, and each lane stores
+//                  its row's 128 outputs straight to global memory (32-byte
+//                  stores when out is 32-byte aligned, else 16-byte ones).
 // Each CTA's tensor core reads the B scales of all 256 columns from its own
 // TMEM, so both CTAs load both w atoms.  TMEM (512 columns, allocated for the
 // pair): accumulators in columns 0-255, the scale factors of ring stage s in
@@ -94,7 +96,7 @@ __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0u;
 }
 
-// Bounded wait; false (and bit 1 of the error word) on timeout.
+// Bounded wait; false (and bit 0 of the error word set) on timeout.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
   if (try_wait(bar, parity)) return true;
   const unsigned long long t0 = gtimer();
