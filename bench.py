@@ -640,6 +640,33 @@ def run_profile_case(args):
                           "mean_launch_ms": round(m, 6),
                           "GB/s": round(Ng * (3 * H + H // 32) / (m * 1e-3) / 1e9, 1)}), flush=True)
         return
+    if args.profile_bwd or args.profile_nvfp4:
+        # the STE backward (x, dy from N(0,1), inv_rms from the forward) or
+        # the NVFP4 pass on the first N rows of the headline workload
+        inv = torch.empty((T,), dtype=torch.float32, device="cuda")
+        if args.profile_bwd:
+            _, _, inv = mx.quant_fwd(x, 2, "mxfp8")
+            gd = torch.Generator(device="cuda").manual_seed(5)
+            dy = torch.randn((T, H), device="cuda", generator=gd).to(torch.bfloat16)
+            dx = torch.empty_like(dy)
+            kernel, nbytes = "mxnorm_bwd_ste", T * (6 * H + 4)
+
+            def fn_k(i):
+                mx.bwd_ste(x, dy, inv, out=dx, stream=stream)
+        else:
+            g = mx.nvfp4_tensor_scale(x)
+            c4 = torch.empty((T, H // 2), dtype=torch.uint8, device="cuda")
+            s4 = torch.empty((T, H // 16), dtype=torch.uint8, device="cuda")
+            kernel, nbytes = "mxnorm_quant_fwd_nvfp4", T * (2 * H + H // 2 + H // 16 + 4)
+
+            def fn_k(i):
+                mx.quant_fwd_nvfp4(x, 2, tensor_scale=g, out=(c4, s4, inv), stream=stream)
+        torch.cuda.synchronize()
+        per, region = time_launches(torch, stream, fn_k, args.steps, args.warmup, 1)
+        m = statistics.fmean(per)
+        print(json.dumps({"profile_only": True, "kernel": kernel, "rows": T, "H": H, "mean_launch_ms": round(m, 6),
+                          "GB/s": round(nbytes / (m * 1e-3) / 1e9, 1)}), flush=True)
+        return
     if args.profile_linear:
         # MXNormLinear's GEMM: the rows quantised with MMA-layout scales
         # against a 4096 x 4096 MXFP8 weight (a Llama-3-8B projection)
@@ -740,6 +767,10 @@ def main():
     ap.add_argument("--profile-linear", action="store_true",
                     help="profiling case: MXNormLinear's GEMM (mxnorm_linear_fwd) on the first N rows "
                          "against a 4096 x 4096 weight")
+    ap.add_argument("--profile-bwd", action="store_true",
+                    help="profiling case: the STE backward (mxnorm_bwd_ste) on the first N rows")
+    ap.add_argument("--profile-nvfp4", action="store_true",
+                    help="profiling case: MXNorm over the NVFP4 cast on the first N rows")
     ap.add_argument("--profile-gain", action="store_true",
                     help="profiling case: the gain-folded MXFP8 weight cast (mx_cast_gain_fwd) of an "
                          "N x 4096 weight")
