@@ -21,7 +21,9 @@ Method sources (by page title and section):
 Parity status of each function is stated in its docstring; all are pinned by
 the ``-m "not gpu"`` tests except the statistical behaviour of the estimator
 (the pages' Theorem 1), which the pages give no constant for: parity
-unpinned there, and no function here claims it.
+unpinned there.  ``theorem1.py`` reports that behaviour as a diagnostic (the
+empirical constant per workload); only the bounds the E8M0 rule forces on it
+are pinned.
 """
 from __future__ import annotations
 

@@ -677,3 +677,37 @@ def test_gain_cast_vs_bruteforce(oracle_mod):
         codes, scales = bf.mx_cast_gain_row([int(b) for b in w[n]], gb, cb)
         assert oc[n].tolist() == codes, n
         assert os_[n].tolist() == scales, n
+
+
+# ------------------------------------------- Theorem 1 diagnostic (bounds)
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "mxfp4_h16", "mxfp8_h16", "mxfp8_h32"])
+@pytest.mark.parametrize("p", [1, 2])
+def test_theorem1_ratio_within_e8m0_bounds(oracle_mod, fmt, p):
+    """RMS_exact * inv_rms lies in the interval the E8M0 rule forces (derived
+    in oracle/theorem1.py from 2^emax s <= amax < 2^(emax+1) s and the
+    block's sum of squares in [amax^2, 32 amax^2]); rotated formats get
+    1e-6 relative slack for the fp32 rounding of the rotation."""
+    from oracle import theorem1
+    from mx_scale_reusing_gb300 import synth
+    for name, rows in (("tiny_64x256", None), ("llama3_125m_16384x768", 1024)):
+        w = synth.WORKLOADS[name]
+        x = synth.make_activations(w, rows=rows)
+        r = theorem1.ratio(x, p, fmt)
+        lo, hi = theorem1.bounds(p, fmt, w.H)
+        slack = 1e-6 if "_h" in fmt else 0.0
+        assert (r >= lo * (1 - slack)).all() and (r < hi * (1 + slack)).all(), (name, r.min(), r.max(), lo, hi)
+
+
+@pytest.mark.parametrize("fmt,emax", [("mxfp8", 8), ("mxfp4", 2)])
+def test_theorem1_ratio_constant_rows(oracle_mod, fmt, emax):
+    """A constant row v gives |v| / 2^(floor(log2 |v|) - emax) for both p,
+    which reaches both ends of the p = 2 bound's top octave."""
+    from oracle import theorem1
+    from mx_scale_reusing_gb300 import synth
+    vals = np.array([1.0, -1.5, 3.0, 0.75, 1.9921875, 2.0 ** -20, 300.0], np.float32)
+    x = synth.f32_to_bf16_bits(np.repeat(vals[:, None], 256, axis=1))
+    v = synth.bf16_bits_to_f32(x[:, 0]).astype(np.float64)
+    want = np.abs(v) / np.exp2(np.floor(np.log2(np.abs(v))) - emax)
+    for p in (1, 2):
+        np.testing.assert_allclose(theorem1.ratio(x, p, fmt), want, rtol=1e-7)
+    assert (want >= 2.0 ** emax).all() and (want < 2.0 ** (emax + 1)).all()
