@@ -28,8 +28,8 @@ For the rotated formats the scales belong to the rotated row, whose RMS is
 x's (H16 / 4 and H32 / sqrt(32) are orthonormal) up to the fp32 rounding of
 the rotation.
 
-Run as a script, it prints the distribution per workload as a Markdown
-table (the table quoted in the design notes was written this way).
+tests/golden/print_theorem1_table.py prints the distribution per workload
+as a Markdown table with summary().
 """
 from __future__ import annotations
 
@@ -66,23 +66,3 @@ def summary(x_bits: np.ndarray, p: int, fmt: str) -> dict:
     r = ratio(x_bits, p, fmt)
     return {"mean": float(r.mean()), "std": float(r.std()), "min": float(r.min()), "max": float(r.max()),
             "cv": float(r.std() / r.mean()), "rows": int(r.size)}
-
-
-def _main():
-    import os
-    import sys
-    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
-    from mx_scale_reusing_gb300 import synth  # seeded input generator only (no method arithmetic)
-    rows_cap = 16384
-    print("| workload | fmt | p | rows | mean | std | cv | min | max |")
-    print("|---|---|---|---|---|---|---|---|---|")
-    for name, w in synth.WORKLOADS.items():
-        x = synth.make_activations(w, rows=min(w.T, rows_cap))
-        for p in (1, 2):
-            s = summary(x, p, w.fmt)
-            print(f"| {name} | {w.fmt} | {p} | {s['rows']} | {s['mean']:.2f} | {s['std']:.2f} | {s['cv']:.4f} | "
-                  f"{s['min']:.2f} | {s['max']:.2f} |")
-
-
-if __name__ == "__main__":
-    _main()
