@@ -540,6 +540,25 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it: the model name where the
+    kernel reports one (x86), else the implementer and part codes (Arm)."""
+    import platform
+    fields = {}
+    try:
+        for line in open("/proc/cpuinfo"):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU implementer" in fields:
+        return f"{platform.machine()} implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    return platform.machine()
+
+
 def oracle_threaded(xb, p, threads):
     """The oracle as it stands over row slices of xb, one slice per thread
     (its C calls release the GIL, so the slices run in parallel)."""
@@ -566,7 +585,7 @@ def cpu_baseline(xb, p, rows):
     oracle_threaded(sample, p, cores)
     dt = time.perf_counter() - t0
     return {"value": round(len(sample) / dt, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "single_thread_tokens_per_s": round(rows / dt1, 1),
+            "cpu": cpu_model(), "single_thread_tokens_per_s": round(rows / dt1, 1),
             "sample": f"first {len(sample)} rows of {WORKLOAD} (H=4096, MXFP8, p={p}) split across {cores} "
                       f"threads, {dt:.2f} s; single-threaded on the first {rows} rows, {dt1:.1f} s"}
 
@@ -601,6 +620,7 @@ def run_reference(args):
             "config": {"workload": WORKLOAD, "T": w.T, "H": w.H, "p": 2, "fmt": "mxfp8_e4m3",
                        "rows_per_step": rows},
             "cpu_baseline": {"value": round(val, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "cpu": cpu_model(),
                              "sample": f"first {rows} rows of {WORKLOAD} per step, split across {cores} threads"},
             "e2e": {"value": round(val, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
