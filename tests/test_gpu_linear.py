@@ -262,3 +262,32 @@ def test_linear_with_gain_folded_weight():
     got = out.float().cpu().numpy().astype(np.float64)
     err = np.abs(got - want)
     assert (err <= 2.0 ** -7 * np.abs(want) + 2.0 ** -12 * np.abs(want).max()).all()
+
+
+def test_linear_matches_cublaslt_mxfp8():
+    """A check that does not go through the oracle: with inv_rms = 1 the
+    kernel is a plain MXFP8 block-scaled GEMM with a bf16 output, which
+    cuBLASLt also computes (torch._scaled_mm with E8M0 scales, read in the
+    same tensor-core scale layout).  Both accumulate in fp32 on the tensor
+    cores, so they agree to the bf16 rounding of the output (bit-equal when
+    the library keeps the same K order); a misread scale layout would be
+    off by powers of two."""
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("this torch has no E8M0 dtype")
+    T, K, N = 2048, 2048, 1024
+    xb = synth.make_random_rows(T, K, seed=31, scale=2.0)
+    wb = synth.make_random_rows(N, K, seed=32, scale=0.03)
+    xc, xs, _ = mx.quant_fwd_mma(dev(xb))
+    wc, ws = mx.mx_cast(dev(wb), "mma")
+    ones = torch.ones((T,), dtype=torch.float32, device="cuda")
+    ours = mx.linear_fwd(xc, xs, ones, wc, ws)
+    try:
+        ref = torch._scaled_mm(xc.view(torch.float8_e4m3fn), wc.view(torch.float8_e4m3fn).t(),
+                               scale_a=xs.view(torch.float8_e8m0fnu), scale_b=ws.view(torch.float8_e8m0fnu),
+                               out_dtype=torch.bfloat16)
+    except (RuntimeError, TypeError, NotImplementedError) as e:
+        pytest.skip(f"cuBLASLt MXFP8 GEMM unavailable: {e}")
+    torch.cuda.synchronize()
+    a, b = ours.double(), ref.double()
+    assert ((a - b).abs() <= 2.0 ** -7 * b.abs() + 2.0 ** -12 * b.abs().max()).all()
+    print(f"bit-equal fraction vs cuBLASLt: {(ours.view(torch.int16) == ref.view(torch.int16)).double().mean().item():.6f}")
