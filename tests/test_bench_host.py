@@ -26,3 +26,29 @@ def test_algorithmic_bytes():
     assert bench.algorithmic_bytes(1, 4096, "mxfp8") == 12420
     assert bench.algorithmic_bytes(1, 4096, "mxfp4") == 10372
     assert bench.baseline_bytes(1, 4096) == 28804
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` (the CPU oracle on the host cores) prints
+    one JSON line with the benchmark contract's keys."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["value"] > 0 and d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["ms_per_step"] > 0 and d["config"]["workload"] == "llama3_8b_65536x4096"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["cpu"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_warmup_below_three_is_refused():
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "2"], capture_output=True, text=True, timeout=120, cwd=ROOT)
+    assert r.returncode != 0 and "warmup" in r.stderr
