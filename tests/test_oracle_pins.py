@@ -711,3 +711,89 @@ def test_theorem1_ratio_constant_rows(oracle_mod, fmt, emax):
     for p in (1, 2):
         np.testing.assert_allclose(theorem1.ratio(x, p, fmt), want, rtol=1e-7)
     assert (want >= 2.0 ** emax).all() and (want < 2.0 ** (emax + 1)).all()
+
+
+# ------------------------------ gain-folded cast: where each rounding falls
+def _fp32_grid_above(v):
+    """Smallest float32 strictly above the positive rational v (normal range)."""
+    from fractions import Fraction as F
+    import math
+    e = math.floor(math.log2(v))
+    if F(2) ** e > v:
+        e -= 1
+    if F(2) ** (e + 1) <= v:
+        e += 1
+    step = F(2) ** (e - 23)
+    k = math.floor(v / step) + 1
+    return k * step
+
+
+def _f32_bits(v) -> int:
+    return int(np.array([float(v)], np.float32).view(np.uint32)[0])
+
+
+def _gain_row(x_bits0, g0, anchor_bits=0x4396):
+    """A 32-element row: element 0 = (x_bits0, gain g0), element 1 = the
+    anchor (300 in bf16 by default) with gain 1, the rest 0 with gain 1.
+    With c * anchor = 300 the block amax is 300 and its scale 2^0."""
+    w = np.zeros((1, 32), np.uint16)
+    w[0, 0] = x_bits0
+    w[0, 1] = anchor_bits
+    g = np.ones(32, np.float32)
+    g[0] = np.float32(float(g0))
+    return w, g
+
+
+def test_gain_cast_each_product_rounds_to_fp32(oracle_mod):
+    """x * g is exactly above the E4M3 tie 17/16 (between 1.0 and 1.125) by
+    less than half an fp32 ulp, so RN_fp32(x * g) = 17/16 and the tie goes to
+    the even code 1.0 (0x38); a product kept exact (or in fp64) would give
+    1.125 (0x39).  The case is found by exact search over bf16 x = 1 + m/128."""
+    from fractions import Fraction as F
+    tie, half_ulp = F(17, 16), F(1, 2 ** 24)
+    for m in range(9, 128):
+        x = F(128 + m, 128)
+        g = _fp32_grid_above(tie / x)
+        if tie < x * g < tie + half_ulp:
+            break
+    else:
+        pytest.fail("no case found")
+    x_bits = 0x3F80 | m  # bf16 of 1 + m/128
+    w, gam = _gain_row(x_bits, g)
+    assert F(float(np.float32(float(g)))) == g
+    codes, scales = oracle_mod.mx_cast_gain(w, gam, 1.0)
+    assert scales[0, 0] == 127 and codes[0, 0] == 0x38
+
+
+def test_gain_cast_gain_rounds_before_the_product(oracle_mod):
+    """g = RN_fp32(c * gamma) is formed first: c = 3 and a gamma whose exact
+    product with c is not an fp32 value, chosen so that x * RN(c * gamma)
+    lands within half an fp32 ulp above the tie 17/16 (RN -> the tie -> 1.0,
+    code 0x38) while the exact x * c * gamma lies above that window and
+    rounds to 1.125 (0x39)."""
+    from fractions import Fraction as F
+    tie, half_ulp = F(17, 16), F(1, 2 ** 24)
+    c = F(3)
+    found = None
+    for m in range(9, 128):
+        x = F(128 + m, 128)
+        # fp32 gains g just above tie / x; gamma = g / 3 rounded to fp32 so
+        # that RN(3 * gamma) = g while 3 * gamma != g
+        g = _fp32_grid_above(tie / x)
+        if not (tie < x * g < tie + half_ulp):
+            continue
+        for gam in (_fp32_grid_above(g / c), _fp32_grid_above(g / c) - F(2) ** -25):
+            cg = c * gam
+            rn = F(float(np.float32(float(cg))))
+            if rn == g and cg != g and x * cg >= tie + half_ulp:
+                found = (m, gam)
+                break
+        if found:
+            break
+    if not found:
+        pytest.skip("no discriminating case in the searched range")
+    m, gam = found
+    w, gvec = _gain_row(0x3F80 | m, gam, anchor_bits=0x42C8)  # 100 * c = 300
+    assert F(float(gvec[0])) == gam
+    codes, scales = oracle_mod.mx_cast_gain(w, gvec, 3.0)
+    assert scales[0, 0] == 127 and codes[0, 0] == 0x38
