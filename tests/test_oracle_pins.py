@@ -797,3 +797,33 @@ def test_gain_cast_gain_rounds_before_the_product(oracle_mod):
     assert F(float(gvec[0])) == gam
     codes, scales = oracle_mod.mx_cast_gain(w, gvec, 3.0)
     assert scales[0, 0] == 127 and codes[0, 0] == 0x38
+
+
+@pytest.mark.parametrize("x,g,tie,code_x", [
+    # RN(3 * RN(1/g)) = 3.5 exactly, the E2M1 tie between 3 and 4 -> even 4 (0x6);
+    # RN(3 / g) = 3.4999998 would give 3 (0x5)
+    (3.0, 0.8571429252624512, 3.5, 0x6),
+    # RN(3.25 * RN(1/g)) = 0.74999994 -> 0.5 (0x1); RN(3.25 / g) = 0.75, the
+    # tie between 0.5 and 1 -> even 1 (0x2)
+    (3.25, 4.333333492279053, 0.75, 0x1),
+])
+def test_nvfp4_elements_scale_by_the_rounded_reciprocal(oracle_mod, x, g, tie, code_x):
+    """The recipe's element step is r = RN(x * enc) with enc = RN(1 / d), not
+    RN(x / d).  Two hand-derived cases where the two readings fall on either
+    side of an E2M1 tie decide it.  The block scale is 1 (the block maximum a
+    = 6g rounded to bf16 gives RN(a / RN(6g)) within an E4M3 half-step of 1),
+    so d = RN(1 * g) = g."""
+    from fractions import Fraction as F
+    from oracle import bruteforce as bf
+    gq = F(float(np.float32(g)))
+    assert gq == F(g)  # g is an fp32 value
+    enc = bf.round_to_fp32(1 / gq)
+    assert (bf.round_to_fp32(F(x) * enc) == tie) != (bf.round_to_fp32(F(x) / gq) == tie)
+    amax = float(synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(np.array([6.0 * g], np.float32)))[0])
+    row = np.zeros((1, 16), np.float32)
+    row[0, 0], row[0, 1] = x, amax
+    xb = synth.f32_to_bf16_bits(row)
+    c, s, _ = oracle_mod.nvfp4_quant(xb, 2, float(np.float32(g)))
+    assert s[0, 0] == 0x38                   # block scale 1.0
+    assert c[0, 0] & 0xF == code_x           # element 0: the product reading's code
+    assert c[0, 0] >> 4 == 0x7               # the block maximum: 6
