@@ -827,3 +827,21 @@ def test_nvfp4_elements_scale_by_the_rounded_reciprocal(oracle_mod, x, g, tie, c
     assert s[0, 0] == 0x38                   # block scale 1.0
     assert c[0, 0] & 0xF == code_x           # element 0: the product reading's code
     assert c[0, 0] >> 4 == 0x7               # the block maximum: 6
+
+
+@pytest.mark.parametrize("n", [16, 32])
+def test_rotation_fp32_values_match_bruteforce(oracle_mod, n):
+    """The rotated fp32 values themselves (not only the codes cast from
+    them) equal the exact-fraction butterfly with the stated stage order and
+    one fp32 rounding per add/sub and per final scale: on general fp32
+    inputs a different stage order or a skipped rounding changes them."""
+    from oracle import bruteforce as bf
+    rng = np.random.default_rng(40 + n)
+    v = (rng.standard_normal((24, n)) * np.exp(rng.normal(0, 3, (24, 1)))).astype(np.float32)
+    v[0] = np.float32(1.0) + np.arange(n, dtype=np.float32) * np.float32(2.0 ** -20)  # rounding in every stage
+    v[1] = (rng.standard_normal(n) * 2.0 ** -124).astype(np.float32)  # products of the 1/4 scale reach subnormals
+    got = (oracle_mod.h16 if n == 16 else oracle_mod.h32)(v.reshape(-1)).reshape(v.shape)
+    rot = bf.h16_fp32 if n == 16 else bf.h32_fp32
+    for r in range(v.shape[0]):
+        want = rot([Fraction(float(a)) for a in v[r]])
+        assert [Fraction(float(a)) for a in got[r]] == want, r
