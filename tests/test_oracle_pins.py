@@ -845,3 +845,40 @@ def test_rotation_fp32_values_match_bruteforce(oracle_mod, n):
     for r in range(v.shape[0]):
         want = rot([Fraction(float(a)) for a in v[r]])
         assert [Fraction(float(a)) for a in got[r]] == want, r
+
+
+def test_nvfp4_block_scale_divides_by_rounded_6g(oracle_mod):
+    """sb = RN(amax / RN(6g)): with amax = 1 and g = 0.10666666 (fp32), RN(6g)
+    makes sb the E4M3 tie 1.5625 exactly, which goes to the even scale 1.5
+    (0x3C); dividing by the exact 6g would give 1.625 (0x3D)."""
+    from fractions import Fraction as F
+    from oracle import bruteforce as bf
+    g = 0.10666666179895401
+    gq = F(g)
+    assert F(float(np.float32(g))) == gq
+    assert bf.round_to_fp32(1 / bf.round_to_fp32(6 * gq)) == F(25, 16)
+    assert bf.nearest_code(bf.round_to_fp32(1 / (6 * gq)), bf._E4M3, 0) == 0x3D
+    row = np.zeros((1, 16), np.float32)
+    row[0, 3] = 1.0
+    _, s, _ = oracle_mod.nvfp4_quant(synth.f32_to_bf16_bits(row), 2, g)
+    assert s[0, 0] == 0x3C
+
+
+def test_nvfp4_reciprocal_of_the_rounded_decode_scale(oracle_mod):
+    """enc = RN(1 / RN(s g)): block scale s = 1.125 (amax 2.4375), g =
+    0.36111107 (fp32), element x = 0.5078125.  With d = RN(s g) the product
+    RN(x * enc) is the E2M1 tie 1.25, which goes to the even 1.0 (0x2); with
+    the exact s g it would give 1.5 (0x3)."""
+    from fractions import Fraction as F
+    from oracle import bruteforce as bf
+    g, x, amax = 0.3611110746860504, 0.5078125, 2.4375
+    gq, s = F(g), F(9, 8)
+    assert F(float(np.float32(g))) == gq
+    rt = bf.round_to_fp32
+    assert bf.nearest_code(rt(F(amax) / rt(6 * gq)), bf._E4M3, 0) == 0x39   # s = 1.125
+    assert rt(F(x) * rt(1 / rt(s * gq))) == F(5, 4)
+    assert bf.nearest_code(rt(F(x) * rt(1 / (s * gq))), bf._E2M1, 0) == 0x3
+    row = np.zeros((1, 16), np.float32)
+    row[0, 0], row[0, 1] = x, amax
+    c, sc, _ = oracle_mod.nvfp4_quant(synth.f32_to_bf16_bits(row), 2, g)
+    assert sc[0, 0] == 0x39 and c[0, 0] & 0xF == 0x2 and c[0, 0] >> 4 == 0x7
