@@ -175,9 +175,12 @@ int mx_cast_gain_fwd(const void* w, int64_t N, int64_t K, const float* gamma, fl
  *   w_codes   E4M3 [N, K]                 16-byte aligned
  *   w_scales  E8M0, MXNORM_SCALE_MMA      mxnorm_mma_scale_bytes(N, K) bytes
  *   out       bf16 [T, N]                 16-byte aligned
- * K % 128 == 0, N % 256 == 0, any T.  Errors and stream semantics as
- * mxnorm_quant_fwd; bit 1 of mxnorm_device_errors reports a timed-out
- * pipeline wait of this kernel. */
+ * K % 128 == 0, K <= MXNORM_MAX_H, N % 256 == 0, N <= 2^24, any T below
+ * 2^31.  The tensor-memory copies address rows with 32-bit coordinates, so
+ * ceil(T/128) * K/32 and ceil(N/128) * K/32 must also stay below 2^31;
+ * larger problems return MXNORM_ERR_UNSUPPORTED before any launch.  Errors
+ * and stream semantics as mxnorm_quant_fwd; bit 1 of mxnorm_device_errors
+ * reports a timed-out pipeline wait of this kernel. */
 int mxnorm_linear_fwd(const void* x_codes, const uint8_t* x_scales, const float* inv_rms, const void* w_codes,
                       const uint8_t* w_scales, int64_t T, int64_t K, int64_t N, void* out, void* stream);
 

@@ -182,6 +182,12 @@ int mxnorm_linear_fwd(const void* x_codes, const uint8_t* x_scales, const float*
   if (K <= 0 || K % 128 != 0) return fail(MXNORM_ERR_INVALID_ARG, "K = %lld is not a positive multiple of 128", (long long)K);
   if (N <= 0 || N % 256 != 0) return fail(MXNORM_ERR_INVALID_ARG, "N = %lld is not a positive multiple of 256", (long long)N);
   if (K > MXNORM_MAX_H || N > (1 << 24)) return fail(MXNORM_ERR_UNSUPPORTED, "K or N too large");
+  // TMA tile coordinates are 32-bit: the rows of x and of the scale maps
+  // (4 per 512-byte atom, K/128 atoms per 128 rows) must stay below 2^31.
+  const int64_t kLimit = int64_t(1) << 31;
+  if (T >= kLimit || ((T + 127) / 128) * (K / 32) >= kLimit || ((N + 127) / 128) * (K / 32) >= kLimit)
+    return fail(MXNORM_ERR_UNSUPPORTED, "T = %lld, N = %lld, K = %lld exceed the 32-bit tile coordinates",
+                (long long)T, (long long)N, (long long)K);
   if (T == 0) return MXNORM_OK;
   if (!x_codes || !x_scales || !inv_rms || !w_codes || !w_scales || !out)
     return fail(MXNORM_ERR_INVALID_ARG, "NULL pointer argument");

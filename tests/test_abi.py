@@ -108,6 +108,11 @@ def test_linear_and_layout_validation(L):
     assert lin(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 128, 128, FAKE, None) == 1
     assert lin(FAKE, FAKE, FAKE, None, FAKE, 8, 128, 256, FAKE, None) == 1
     assert lin(FAKE, FAKE + 8, FAKE, FAKE, FAKE, 8, 128, 256, FAKE, None) == 3
+    # 32-bit tile coordinates: too many rows, or too many scale-map rows
+    assert lin(FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 31, 128, 256, FAKE, None) == 2
+    assert lin(FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 28, 1 << 15, 256, FAKE, None) == 2  # 2^21 tiles x 2^10
+    assert lin(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 1 << 20, 1 << 24, FAKE, None) == 2
+    assert lin(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1 << 15, 1 << 12, FAKE, None) == 0
     q = L.mxnorm_quant_fwd_layout
     assert q(FAKE, 8, 96, 2, 0, FAKE, FAKE, FAKE, 1, None) == 1
     assert q(FAKE, 8, 128, 2, 0, FAKE, FAKE, FAKE, 7, None) == 1
