@@ -101,6 +101,23 @@ def _stream_ptr(device, stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _require(t, name: str, device, dtype=None, min_numel: int = 0, byte_elems: bool = False):
+    """Raise ValueError unless t is a contiguous CUDA tensor on `device` with
+    dtype `dtype` (or 1-byte elements when byte_elems) and at least
+    min_numel elements: the C ABI takes bare pointers and cannot check how
+    large a buffer is."""
+    if not (getattr(t, "is_cuda", False) and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if byte_elems and t.element_size() != 1:
+        raise ValueError(f"{name} must have 1-byte elements (uint8 or an 8-bit float)")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, not {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call's tensors are on {device}")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, the call writes or reads {min_numel}")
+
+
 def mxnorm_quant_fwd(x_ptr: int, T: int, H: int, p: int, fmt: int, codes_ptr: int, scales_ptr: int,
                      inv_rms_ptr: int, stream_ptr: int = 0, variant: int = 0) -> None:
     """Raw C-ABI call on device pointers (ints); raises MXNormError."""
@@ -127,9 +144,13 @@ def quant_fwd(x, p: int = 2, fmt: str = "mxfp8", variant: str = "auto", out=None
         inv = torch.empty(lead, dtype=torch.float32, device=x.device)
     else:
         codes, scales, inv = out
-    _check(lib().mxnorm_quant_fwd_ex(x.data_ptr(), T, H, int(p), FMT[fmt], codes.data_ptr(),
-                                     scales.data_ptr(), inv.data_ptr(), VARIANT[variant],
-                                     _stream_ptr(x.device, stream)))
+        _require(codes, "codes", x.device, min_numel=T * code_bytes(H, fmt), byte_elems=True)
+        _require(scales, "scales", x.device, min_numel=T * (H // 32), byte_elems=True)
+        _require(inv, "inv_rms", x.device, torch.float32, T)
+    with torch.cuda.device(x.device):
+        _check(lib().mxnorm_quant_fwd_ex(x.data_ptr(), T, H, int(p), FMT[fmt], codes.data_ptr(),
+                                         scales.data_ptr(), inv.data_ptr(), VARIANT[variant],
+                                         _stream_ptr(x.device, stream)))
     return codes, scales, inv
 
 
@@ -149,8 +170,13 @@ def rmsnorm_mxfp8_ref_fwd(x, eps: float = 1e-5, out=None, stream=None):
         inv = torch.empty(lead, dtype=torch.float32, device=x.device)
     else:
         y, codes, scales, inv = out
-    _check(lib().rmsnorm_mxfp8_ref_fwd(x.data_ptr(), T, H, float(eps), y.data_ptr(), codes.data_ptr(),
-                                       scales.data_ptr(), inv.data_ptr(), _stream_ptr(x.device, stream)))
+        _require(y, "y", x.device, torch.bfloat16, T * H)
+        _require(codes, "codes", x.device, min_numel=T * H, byte_elems=True)
+        _require(scales, "scales", x.device, min_numel=T * (H // 32), byte_elems=True)
+        _require(inv, "inv_rms", x.device, torch.float32, T)
+    with torch.cuda.device(x.device):
+        _check(lib().rmsnorm_mxfp8_ref_fwd(x.data_ptr(), T, H, float(eps), y.data_ptr(), codes.data_ptr(),
+                                           scales.data_ptr(), inv.data_ptr(), _stream_ptr(x.device, stream)))
     return y, codes, scales, inv
 
 
@@ -161,7 +187,8 @@ def absmax(x, stream=None):
     if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
         raise ValueError("x must be a contiguous bfloat16 CUDA tensor")
     out = torch.empty((1,), dtype=torch.float32, device=x.device)
-    _check(lib().mxnorm_absmax_bf16(x.data_ptr(), x.numel(), out.data_ptr(), _stream_ptr(x.device, stream)))
+    with torch.cuda.device(x.device):
+        _check(lib().mxnorm_absmax_bf16(x.data_ptr(), x.numel(), out.data_ptr(), _stream_ptr(x.device, stream)))
     return out
 
 
@@ -190,8 +217,12 @@ def quant_fwd_nvfp4(x, p: int = 2, tensor_scale=None, out=None, stream=None):
                torch.empty(lead + (H // 16,), dtype=torch.uint8, device=x.device),
                torch.empty(lead, dtype=torch.float32, device=x.device))
     codes, scales, inv = out
-    _check(lib().mxnorm_quant_fwd_nvfp4(x.data_ptr(), T, H, int(p), g, codes.data_ptr(), scales.data_ptr(),
-                                        inv.data_ptr(), _stream_ptr(x.device, stream)))
+    _require(codes, "codes", x.device, min_numel=T * (H // 2), byte_elems=True)
+    _require(scales, "scales", x.device, min_numel=T * (H // 16), byte_elems=True)
+    _require(inv, "inv_rms", x.device, torch.float32, T)
+    with torch.cuda.device(x.device):
+        _check(lib().mxnorm_quant_fwd_nvfp4(x.data_ptr(), T, H, int(p), g, codes.data_ptr(), scales.data_ptr(),
+                                            inv.data_ptr(), _stream_ptr(x.device, stream)))
     return codes, scales, inv
 
 
@@ -224,8 +255,9 @@ def quant_fwd_mma(x, p: int = 2, fmt: str = "mxfp8", stream=None):
     codes = torch.empty(tuple(x.shape[:-1]) + (code_bytes(H, fmt),), dtype=torch.uint8, device=x.device)
     scales = _scale_buffer(T, H, "mma", x.device)
     inv = torch.empty(tuple(x.shape[:-1]), dtype=torch.float32, device=x.device)
-    _check(lib().mxnorm_quant_fwd_layout(x.data_ptr(), T, H, int(p), FMT[fmt], codes.data_ptr(), scales.data_ptr(),
-                                         inv.data_ptr(), 1, _stream_ptr(x.device, stream)))
+    with torch.cuda.device(x.device):
+        _check(lib().mxnorm_quant_fwd_layout(x.data_ptr(), T, H, int(p), FMT[fmt], codes.data_ptr(),
+                                             scales.data_ptr(), inv.data_ptr(), 1, _stream_ptr(x.device, stream)))
     return codes, scales, inv
 
 
@@ -238,8 +270,9 @@ def mx_cast(x, layout: str = "row_major", stream=None):
     T = x.numel() // H if H else 0
     codes = torch.empty(tuple(x.shape), dtype=torch.uint8, device=x.device)
     scales = _scale_buffer(T, H, layout, x.device)
-    _check(lib().mx_cast_fwd(x.data_ptr(), T, H, 0, codes.data_ptr(), scales.data_ptr(), SCALE_LAYOUT[layout],
-                             _stream_ptr(x.device, stream)))
+    with torch.cuda.device(x.device):
+        _check(lib().mx_cast_fwd(x.data_ptr(), T, H, 0, codes.data_ptr(), scales.data_ptr(), SCALE_LAYOUT[layout],
+                                 _stream_ptr(x.device, stream)))
     return codes, scales
 
 
@@ -252,12 +285,14 @@ def mx_cast_gain(w, gamma, c: float = 1.0, layout: str = "mma", stream=None):
     if not (w.is_cuda and w.dtype == torch.bfloat16 and w.is_contiguous() and w.dim() == 2):
         raise ValueError("w must be a contiguous 2-D bfloat16 CUDA tensor")
     N, K = w.shape
-    if not (gamma.is_cuda and gamma.dtype == torch.float32 and gamma.is_contiguous() and gamma.shape == (K,)):
-        raise ValueError("gamma must be a contiguous float32 CUDA tensor of K entries")
+    _require(gamma, "gamma", w.device, torch.float32)
+    if tuple(gamma.shape) != (K,):
+        raise ValueError("gamma must hold K entries")
     codes = torch.empty((N, K), dtype=torch.uint8, device=w.device)
     scales = _scale_buffer(N, K, layout, w.device)
-    _check(lib().mx_cast_gain_fwd(w.data_ptr(), N, K, gamma.data_ptr(), float(c), codes.data_ptr(),
-                                  scales.data_ptr(), SCALE_LAYOUT[layout], _stream_ptr(w.device, stream)))
+    with torch.cuda.device(w.device):
+        _check(lib().mx_cast_gain_fwd(w.data_ptr(), N, K, gamma.data_ptr(), float(c), codes.data_ptr(),
+                                      scales.data_ptr(), SCALE_LAYOUT[layout], _stream_ptr(w.device, stream)))
     return codes, scales
 
 
@@ -265,12 +300,26 @@ def linear_fwd(x_codes, x_scales, inv_rms, w_codes, w_scales, out=None, stream=N
     """MXNormLinear's consumer GEMM on the tensor cores: out = bf16(inv_rms[t]
     * sum_k x^[t,k] w^[n,k]); scales in the MMA layout.  Returns out [T, N]."""
     import torch
+    if getattr(x_codes, "dim", lambda: 0)() != 2 or getattr(w_codes, "dim", lambda: 0)() != 2:
+        raise ValueError("x_codes and w_codes must be 2-D [rows, K]")
     T, K = x_codes.shape
     N = w_codes.shape[0]
+    if w_codes.shape[1] != K:
+        raise ValueError(f"w_codes has K = {w_codes.shape[1]}, x_codes has K = {K}")
+    dev = x_codes.device
+    _require(x_codes, "x_codes", dev, byte_elems=True)
+    _require(w_codes, "w_codes", dev, byte_elems=True)
+    if K % 128 == 0:  # else the C ABI reports the shape error
+        _require(x_scales, "x_scales", dev, min_numel=mma_scale_bytes(T, K), byte_elems=True)
+        _require(w_scales, "w_scales", dev, min_numel=mma_scale_bytes(N, K), byte_elems=True)
+    _require(inv_rms, "inv_rms", dev, torch.float32, T)
     if out is None:
-        out = torch.empty((T, N), dtype=torch.bfloat16, device=x_codes.device)
-    _check(lib().mxnorm_linear_fwd(x_codes.data_ptr(), x_scales.data_ptr(), inv_rms.data_ptr(), w_codes.data_ptr(),
-                                   w_scales.data_ptr(), T, K, N, out.data_ptr(), _stream_ptr(x_codes.device, stream)))
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    _require(out, "out", dev, torch.bfloat16, T * N)
+    with torch.cuda.device(dev):
+        _check(lib().mxnorm_linear_fwd(x_codes.data_ptr(), x_scales.data_ptr(), inv_rms.data_ptr(),
+                                       w_codes.data_ptr(), w_scales.data_ptr(), T, K, N, out.data_ptr(),
+                                       _stream_ptr(dev, stream)))
     return out
 
 
@@ -288,14 +337,19 @@ def bwd_ste(x, dy, inv_rms, out=None, stream=None):
     T = x.numel() // H if H else 0
     if inv_rms.numel() != T:
         raise ValueError("inv_rms needs one value per row")
+    _require(dy, "dy", x.device)
+    _require(inv_rms, "inv_rms", x.device, torch.float32, T)
     dx = torch.empty_like(x) if out is None else out
-    _check(lib().mxnorm_bwd_ste(x.data_ptr(), dy.data_ptr(), inv_rms.data_ptr(), T, H, dx.data_ptr(),
-                                _stream_ptr(x.device, stream)))
+    _require(dx, "out", x.device, torch.bfloat16, T * H)
+    with torch.cuda.device(x.device):
+        _check(lib().mxnorm_bwd_ste(x.data_ptr(), dy.data_ptr(), inv_rms.data_ptr(), T, H, dx.data_ptr(),
+                                    _stream_ptr(x.device, stream)))
     return dx
 
 
 def device_errors(clear: bool = True) -> int:
-    """The device error word (bit 0: a bounded pipeline wait timed out)."""
+    """The device error flags: bit 0, a bounded wait of the tiled kernel
+    timed out; bit 1, a pipeline wait of the GEMM timed out."""
     v = ctypes.c_uint32(0)
     _check(lib().mxnorm_device_errors(ctypes.byref(v), int(clear)))
     return v.value

@@ -157,3 +157,54 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(mx, "library_path", str(tmp_path / "absent.so"))
     with pytest.raises(mx.MXNormLibraryMissing):
         mx.lib()
+
+
+class _FakeCuda:
+    """Stands in for a CUDA tensor in the binding's argument checks (no GPU
+    here): the attributes _require reads."""
+
+    def __init__(self, numel, dtype, device="cuda:0", contiguous=True, esize=None):
+        import torch
+        self._n, self.dtype, self.device = numel, dtype, torch.device(device)
+        self.is_cuda, self._c = True, contiguous
+        self._es = esize if esize is not None else torch.empty((), dtype=dtype).element_size()
+
+    def is_contiguous(self):
+        return self._c
+
+    def numel(self):
+        return self._n
+
+    def element_size(self):
+        return self._es
+
+
+def test_binding_buffer_checks():
+    """Buffers handed to the C ABI are checked for device, dtype, layout and
+    size before any call: the ABI takes bare pointers."""
+    import torch
+    d0 = torch.device("cuda:0")
+    ok = _FakeCuda(100, torch.float32)
+    mx._require(ok, "inv_rms", d0, torch.float32, 100)
+    with pytest.raises(ValueError, match="holds 99"):
+        mx._require(_FakeCuda(99, torch.float32), "inv_rms", d0, torch.float32, 100)
+    with pytest.raises(ValueError, match="must be torch.float32"):
+        mx._require(_FakeCuda(100, torch.float16), "inv_rms", d0, torch.float32, 100)
+    with pytest.raises(ValueError, match="is on cuda:1"):
+        mx._require(_FakeCuda(100, torch.float32, "cuda:1"), "inv_rms", d0, torch.float32, 100)
+    with pytest.raises(ValueError, match="contiguous"):
+        mx._require(_FakeCuda(100, torch.float32, contiguous=False), "inv_rms", d0, torch.float32)
+    with pytest.raises(ValueError, match="1-byte"):
+        mx._require(_FakeCuda(100, torch.int16), "codes", d0, byte_elems=True)
+    mx._require(_FakeCuda(100, torch.uint8), "codes", d0, byte_elems=True, min_numel=100)
+    with pytest.raises(ValueError, match="contiguous CUDA"):
+        mx._require(torch.zeros(4), "x", d0)
+
+
+def test_binding_rejects_host_tensors():
+    import torch
+    x = torch.zeros((4, 32), dtype=torch.bfloat16)
+    for fn in (lambda: mx.quant_fwd(x), lambda: mx.mx_cast(x), lambda: mx.quant_fwd_mma(x),
+               lambda: mx.mx_cast_gain(x, torch.ones(32)), lambda: mx.bwd_ste(x, x, torch.ones(4))):
+        with pytest.raises(ValueError):
+            fn()
