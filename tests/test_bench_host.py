@@ -52,3 +52,24 @@ def test_warmup_below_three_is_refused():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
                         "--warmup", "2"], capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched the way a multi-GPU run is (torchrun, two ranks), the
+    reference arm runs on rank 0 alone and prints one JSON line; the other
+    rank exits 0 without work."""
+    import json
+    import socket
+    import subprocess
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    assert json.loads(lines[0])["impl"] == "reference"
