@@ -586,6 +586,7 @@ def cpu_baseline(xb, p, rows):
     dt = time.perf_counter() - t0
     return {"value": round(len(sample) / dt, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "cpu": cpu_model(), "single_thread_tokens_per_s": round(rows / dt1, 1),
+            "GB/s": round(len(sample) / dt * algorithmic_bytes(1, xb.shape[1], "mxfp8") / 1e9, 3),
             "sample": f"first {len(sample)} rows of {WORKLOAD} (H=4096, MXFP8, p={p}) split across {cores} "
                       f"threads, {dt:.2f} s; single-threaded on the first {rows} rows, {dt1:.1f} s"}
 
@@ -620,7 +621,7 @@ def run_reference(args):
             "config": {"workload": WORKLOAD, "T": w.T, "H": w.H, "p": 2, "fmt": "mxfp8_e4m3",
                        "rows_per_step": rows},
             "cpu_baseline": {"value": round(val, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "cpu": cpu_model(),
+                             "cpu": cpu_model(), "GB/s": round(val * algorithmic_bytes(1, w.H, "mxfp8") / 1e9, 3),
                              "sample": f"first {rows} rows of {WORKLOAD} per step, split across {cores} threads"},
             "e2e": {"value": round(val, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -73,3 +73,15 @@ def test_reference_arm_under_torchrun_prints_once():
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
     assert json.loads(lines[0])["impl"] == "reference"
+
+
+def test_cpu_baseline_fields():
+    """The GPU arm's cpu_baseline block (the oracle on the host cores, on a
+    bounded sample) carries the keys the benchmark line needs."""
+    from mx_scale_reusing_gb300 import synth
+    xb = synth.make_activations(synth.WORKLOADS["llama3_8b_65536x4096"], rows=512)
+    cb = bench.cpu_baseline(xb, 2, 64)
+    assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s" and cb["cores"] >= 1 and cb["cpu"]
+    assert cb["value"] > 0 and cb["single_thread_tokens_per_s"] > 0
+    assert abs(cb["GB/s"] - cb["value"] * 12420 / 1e9) <= 1e-3 + 1e-3 * cb["GB/s"]
+    assert "rows" in cb["sample"]
