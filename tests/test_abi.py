@@ -208,3 +208,39 @@ def test_binding_rejects_host_tensors():
                lambda: mx.mx_cast_gain(x, torch.ones(32)), lambda: mx.bwd_ste(x, x, torch.ones(4))):
         with pytest.raises(ValueError):
             fn()
+
+
+def test_header_is_plain_c_and_links(L):
+    """include/mxnorm.h compiles as strict C11 with nothing but the C
+    library, and a C program that takes every declared entry point links
+    against libmxnorm.so and runs its host-only calls."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    work = os.path.join(ROOT, "_build", "c_abi_check")
+    os.makedirs(work, exist_ok=True)
+    src = os.path.join(work, "use_mxnorm.c")
+    with open(src, "w") as f:
+        f.write('#include "mxnorm.h"\n#include <stdio.h>\n#include <string.h>\n'
+                "typedef void (*fn_t)(void);\n"
+                "static const fn_t entry_points[] = {\n"
+                + "".join(f"    (fn_t){n},\n" for n in names)
+                + "};\n"
+                "int main(void) {\n"
+                '    printf("%d %d %s|%s\\n", mxnorm_abi_version(), (int)(sizeof entry_points / sizeof entry_points[0]),\n'
+                "           mxnorm_status_string(MXNORM_ERR_INVALID_ARG), mxnorm_last_error());\n"
+                "    return 0;\n}\n")
+    libdir = os.path.dirname(mx.library_path)
+    exe = os.path.join(work, "use_mxnorm")
+    r = subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                        src, "-L", libdir, "-l:" + os.path.basename(mx.library_path), "-Wl,-rpath," + libdir,
+                        "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    version, count, rest = r.stdout.split(" ", 2)
+    assert int(version) == L.mxnorm_abi_version() and int(count) == len(names)
+    assert rest.startswith(L.mxnorm_status_string(1).decode())
