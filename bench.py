@@ -46,12 +46,15 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "mxnorm_warp_row_llama3_8b_6553
 
 
 def algorithmic_bytes(T: int, H: int, fmt: str) -> int:
+    """Bytes the fused pass must move for T rows: 2H read, the codes, H/32
+    scales and a 4-byte inv_rms per row."""
     code = H if fmt == "mxfp8" else H // 2
     return T * (2 * H + code + H // 32 + 4)
 
 
 def baseline_bytes(T: int, H: int) -> int:
-    # kernel 1: read x, write y, write inv; kernel 2: read y, write codes + scales
+    """Bytes of the two-pass baseline: kernel 1 reads x and writes y and
+    inv_rms, kernel 2 reads y and writes codes and scales."""
     return T * (2 * H + 2 * H + 4) + T * (2 * H + H + H // 32)
 
 
@@ -89,6 +92,7 @@ def profiled_traffic():
 
 
 def measured_peaks():
+    """(peaks dict, "measured") from MEASURED_PEAKS.json, else ({}, "fallback")."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             return json.load(f), "measured"
@@ -170,6 +174,8 @@ def time_launches(torch, stream, fn, steps: int, warmup: int, nbuf: int):
 
 
 def run_gpu(args):
+    """The benchmark on this rank's GPU: the timed headline pass, the
+    secondary legs, the end-to-end leg and (rank 0) the JSON line."""
     import torch
     import torch.distributed as dist
 
@@ -515,6 +521,8 @@ def run_gpu(args):
 
 
 def run_e2e(torch, mx, x_host, T, H, dev, steps):
+    """End to end through the public API from pinned host buffers: every
+    timed step moves x in and the codes, scales and inv_rms out."""
     x_pin = x_host.pin_memory()
     c_pin = torch.empty((T, H), dtype=torch.uint8).pin_memory()
     s_pin = torch.empty((T, H // 32), dtype=torch.uint8).pin_memory()
@@ -534,6 +542,7 @@ def run_e2e(torch, mx, x_host, T, H, dev, steps):
 
 
 def host_cores() -> int:
+    """Host cores this process may run on."""
     try:
         return len(os.sched_getaffinity(0))
     except (AttributeError, OSError):
@@ -767,6 +776,8 @@ def run_shape_sweep(args):
 
 
 def main():
+    """Command line: the benchmark (default), the reference arm, the
+    profiling cases or the shape sweep."""
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)

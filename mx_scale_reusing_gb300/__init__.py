@@ -34,10 +34,14 @@ _lib = None
 
 
 class MXNormLibraryMissing(RuntimeError):
-    pass
+    """libmxnorm.so is not built: every call raises this (there is no CPU
+    fallback)."""
 
 
 class MXNormError(RuntimeError):
+    """A C-ABI call returned a non-zero mxnorm_status; `status` holds it and
+    the message is the library's mxnorm_last_error() text."""
+
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS.get(status, status)}: {message}")
         self.status = status
@@ -92,6 +96,8 @@ def _check(status: int):
 
 
 def code_bytes(H: int, fmt: str) -> int:
+    """Bytes of codes per row of H elements: one per E4M3 code, one per two
+    E2M1 codes."""
     return H if fmt.startswith("mxfp8") else H // 2
 
 

@@ -34,6 +34,9 @@ CHUNK_ROWS = 1024
 
 @dataclass(frozen=True)
 class Workload:
+    """One seeded synthetic activation workload: T rows of H bf16 values
+    drawn from `dist` with per-channel gains and `outlier_frac` of the
+    channels (or the listed `outlier_channels`) scaled by `outlier_gain`."""
     name: str
     T: int
     H: int
@@ -48,6 +51,7 @@ class Workload:
 
     @property
     def K(self) -> int:
+        """MX blocks per row."""
         return self.H // 32
 
 
@@ -79,10 +83,14 @@ def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> their float32 values (exact)."""
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
 def channel_gains(w: Workload, rng: np.random.Generator) -> np.ndarray:
+    """Per-channel gains shared by every row of w: exp(0.5 Z) times the
+    outlier gain on the outlier channels (a seeded permutation), or ones
+    with the listed outlier channels for the normal workload."""
     H = w.H
     if w.dist == "normal":
         g = np.ones(H, np.float32)

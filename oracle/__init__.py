@@ -112,6 +112,7 @@ def _as_bf16_bits(x) -> np.ndarray:
 
 
 def code_bytes_per_row(H: int, fmt) -> int:
+    """Code bytes of one row: H for the FP8 formats, H/2 for FP4."""
     return H if _fmt_id(fmt) in FP8_FMTS else H // 2
 
 
@@ -294,8 +295,10 @@ def float_to_bf16(v) -> np.ndarray:
 
 
 def decode_e4m3(code: int) -> float:
+    """Value of an E4M3 code byte (OCP MX v1.0, section 5.3)."""
     return _load().oracle_decode_e4m3(int(code))
 
 
 def decode_e2m1(nibble: int) -> float:
+    """Value of an E2M1 code nibble (OCP MX v1.0, section 5.3)."""
     return _load().oracle_decode_e2m1(int(nibble))
