@@ -1,7 +1,8 @@
 """Host-side checks of bench.py (no GPU): the committed ncu summary of the
-headline kernel matches the current kernel sources, so the bench's
-roofline reports the measured DRAM traffic rather than null; and the
-algorithmic byte counts per row follow from the tensor sizes."""
+headline kernel matches the current kernel sources (so the roofline
+reports the measured DRAM traffic rather than null); the algorithmic byte
+counts; the reference arm's JSON line, alone and under torchrun with two
+ranks; the warm-up floor; and the CPU-baseline block of the GPU arm."""
 import os
 import sys
 
