@@ -539,6 +539,52 @@ def test_bwd_closed_forms(oracle_mod):
     assert np.abs(dx[1]).max() <= 1e-6
 
 
+@pytest.mark.parametrize("a", [-100, -60, -40, 50, 60])
+def test_bwd_scale_equivariance_at_extreme_row_scales(oracle_mod, a):
+    """dx(2^a x, dy, 2^-a r) = 2^-a dx(x, dy, r) exactly: every term of
+    r dy - r^3 x mean(dy x) scales by 2^-a, so the unrounded result must too
+    (fp64 keeps the products of such rows far from its own range limits).
+    Pins the oracle on rows whose amax is near 2^-100 .. 2^60 against its
+    values on ordinary rows."""
+    T, H = 4, 256
+    x = synth.make_random_rows(T, H, seed=31, scale=2.0)
+    dy = synth.make_random_rows(T, H, seed=32)
+    inv = np.array([0.5, 0.75, 1.25, 3.0], np.float32)
+    xs = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(x) * np.float32(2.0 ** a))
+    assert np.array_equal(synth.bf16_bits_to_f32(xs), synth.bf16_bits_to_f32(x) * np.float32(2.0 ** a))
+    _, ref = oracle_mod.mxnorm_bwd_ste(x, dy, inv, with_f64=True)
+    _, got = oracle_mod.mxnorm_bwd_ste(xs, dy, (inv * np.float32(2.0 ** -a)).astype(np.float32), with_f64=True)
+    assert np.array_equal(got, ref * 2.0 ** -a)
+
+
+def test_bwd_zero_and_subnormal_rows_exact(oracle_mod):
+    """The two rows whose forward estimate is the largest, 2^127: an all-zero
+    row gives dx = 2^127 dy exactly (bf16 Inf where that exceeds the bf16
+    range), and a row of bf16 subnormals matches the definition evaluated in
+    exact rationals (fp64's rounding stays below 2^-50 of the largest term)."""
+    from oracle import bruteforce as bf
+    H = 64
+    r = np.float32(2.0 ** 127)
+    dyb = synth.make_random_rows(2, H, seed=33)
+    xb = np.zeros((2, H), np.uint16)
+    xb[1] = (np.arange(H, dtype=np.uint16) * 37) % 0x7F + 1
+    xb[1, ::3] |= np.uint16(0x8000)
+    dx, dx64 = oracle_mod.mxnorm_bwd_ste(xb, dyb, np.array([r, r], np.float32), with_f64=True)
+    dyv = synth.bf16_bits_to_f32(dyb[0]).astype(np.float64)
+    assert np.array_equal(dx64[0], dyv * 2.0 ** 127)
+    big = np.abs(dyv) * 2.0 ** 127 >= (2 - 2.0 ** -8) * 2.0 ** 127
+    assert ((dx[0] & 0x7FFF) == 0x7F80)[big].all()
+    assert np.array_equal(dx[0][~big], dyb[0][~big] + np.uint16(127 << 7))
+    rq = Fraction(2) ** 127
+    xs = [bf.bf16_value(int(b)) for b in xb[1]]
+    gs = [bf.bf16_value(int(b)) for b in dyb[1]]
+    dot = sum(g * v for g, v in zip(gs, xs))
+    exact = [rq * g - rq ** 3 * v * dot / H for g, v in zip(gs, xs)]
+    scale = max(abs(rq * g) for g in gs) + max(abs(rq ** 3 * v * dot / H) for v in xs)
+    for j in range(H):
+        assert abs(Fraction(float(dx64[1, j])) - exact[j]) <= scale * Fraction(1, 2 ** 50), j
+
+
 # ------------------------------------------------------------------ NVFP4
 def _f32_bits(v):
     import struct
