@@ -89,8 +89,17 @@ static float bf16_bits_to_float(uint16_t b)
     return f;
 }
 
+/* Magnitude of a non-negative bf16 pattern, with the pattern above bf16 max
+ * (0x7F80) read as 2^128: the value round-to-nearest compares against
+ * before it overflows to Inf (IEEE 754-2019, 4.3.1 and 7.4). */
+static double bf16_magnitude_unbounded(uint16_t b)
+{
+    return (b & 0x7FFFu) == 0x7F80u ? ldexp(1.0, 128) : fabs((double)bf16_bits_to_float(b));
+}
+
 /* Round a float to the nearest bf16, ties to an even last bit, by comparing
- * the two bf16 neighbours of f exactly (in double). */
+ * the two bf16 neighbours of f exactly (in double); beyond bf16 max + half
+ * an ulp it overflows to Inf. */
 static uint16_t float_to_bf16_rne(float f)
 {
     uint32_t u;
@@ -100,7 +109,7 @@ static uint16_t float_to_bf16_rne(float f)
     if ((u & 0xFFFFu) == 0) return lo;
     uint16_t hi = (uint16_t)(lo + 1);                     /* next magnitude up */
     double dlo = fabs((double)bf16_bits_to_float(lo));
-    double dhi = fabs((double)bf16_bits_to_float(hi));   /* may be inf */
+    double dhi = bf16_magnitude_unbounded(hi);
     double a = fabs((double)f);
     double dist_lo = a - dlo, dist_hi = dhi - a;
     if (dist_lo < dist_hi) return lo;
@@ -108,12 +117,15 @@ static uint16_t float_to_bf16_rne(float f)
     return (lo & 1u) ? hi : lo;
 }
 
-/* Round a double to the nearest bf16 (ties to an even last bit); finite
- * values within the bf16 range only.  The two bf16 neighbours are found
- * from the float nearest below in magnitude and compared exactly. */
+/* Round a double to the nearest bf16 (ties to an even last bit), IEEE 754
+ * style: a magnitude from bf16 max + half an ulp (2^128 - 2^119, a tie that
+ * goes to the even neighbour 2^128) upwards overflows to Inf.  The two bf16
+ * neighbours are found from the float nearest below in magnitude and
+ * compared exactly. */
 static uint16_t double_to_bf16_rne(double d)
 {
     if (isnan(d)) return 0x7FC0;
+    if (isinf(d)) return (uint16_t)(signbit(d) ? 0xFF80u : 0x7F80u);
     double a = fabs(d);
     /* largest bf16 magnitude <= a: truncate the float of a toward zero */
     float f = (float)a;
@@ -124,7 +136,7 @@ static uint16_t double_to_bf16_rne(double d)
     if ((double)bf16_bits_to_float(lo) > a) lo = (uint16_t)(lo - 1);
     uint16_t hi = (uint16_t)(lo + 1);
     double dlo = a - (double)bf16_bits_to_float(lo);
-    double dhi = (double)bf16_bits_to_float(hi) - a;
+    double dhi = bf16_magnitude_unbounded(hi) - a;
     uint16_t m = (dlo < dhi) ? lo : (dhi < dlo) ? hi : ((lo & 1u) ? hi : lo);
     if (dlo == 0.0) m = lo;
     return (uint16_t)(m | (signbit(d) ? 0x8000u : 0u));
