@@ -87,6 +87,8 @@ def _load():
     lib.oracle_mxfp8_linear.argtypes = [p, p, p, p, p, i64, i64, i64, p]
     lib.oracle_mxfp8_linear.restype = i32
     lib.oracle_nvfp4_rows.restype = i32
+    lib.oracle_nvfp4_tensor_scale.argtypes = [p, i64]
+    lib.oracle_nvfp4_tensor_scale.restype = f32
     lib.oracle_mxnorm_bwd_ste_rows.restype = i32
     lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
     lib.oracle_decode_e4m3.restype = ctypes.c_double
@@ -94,6 +96,32 @@ def _load():
     lib.oracle_decode_e2m1.restype = ctypes.c_double
     _lib = lib
     return lib
+
+
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def rows_in_threads(fn, *row_arrays, threads: int | None = None):
+    """fn(*slices) over slices of the row arrays (split along axis 0), one
+    slice per host thread, results concatenated along rows (each output
+    array of a tuple separately).  The oracle's C calls release the GIL, so
+    the slices run on separate cores; every row is still computed exactly
+    as one call over all rows would compute it (rows are independent)."""
+    from concurrent.futures import ThreadPoolExecutor
+    n = row_arrays[0].shape[0]
+    k = max(1, min(threads or host_threads(), n))
+    bounds = np.linspace(0, n, k + 1).astype(np.int64)
+    parts = [tuple(np.ascontiguousarray(a[lo:hi]) for a in row_arrays) for lo, hi in zip(bounds[:-1], bounds[1:])]
+    with ThreadPoolExecutor(max_workers=k) as ex:
+        outs = list(ex.map(lambda args: fn(*args), parts))
+    if isinstance(outs[0], tuple):
+        return tuple(np.concatenate([o[i] for o in outs]) for i in range(len(outs[0])))
+    return np.concatenate(outs)
 
 
 def _ptr(a: np.ndarray):
@@ -214,6 +242,13 @@ def nvfp4_quant(x_bits: np.ndarray, p: int, tensor_scale: float):
     if lib.oracle_nvfp4_rows(_ptr(x), T, H, int(p), float(tensor_scale), _ptr(codes), _ptr(scales), _ptr(inv)) != 0:
         raise ValueError("oracle rejected arguments")
     return codes, scales, inv
+
+
+def nvfp4_tensor_scale(x_bits: np.ndarray) -> float:
+    """The NVFP4 tensor scale of a bf16 tensor: RN_fp32(a / (448 * 6)) with
+    a the largest finite |x|, 1.0 when there is none but zero."""
+    x = _as_bf16_bits(x_bits)
+    return float(_load().oracle_nvfp4_tensor_scale(_ptr(x), x.size))
 
 
 def mxnorm_bwd_ste(x_bits: np.ndarray, dy_bits: np.ndarray, inv_rms: np.ndarray, with_f64: bool = False):

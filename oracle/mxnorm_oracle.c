@@ -52,7 +52,10 @@
  *     sat_RNE_E2M1(r_j).  The estimator's m~_k is the block's decode scale
  *     s_k * g; inv_rms = ((1/K) sum_k (s_k g)^p)^(-1/p), K = H/16, +Inf when
  *     every s_k is 0.  A block with Inf/NaN: scale code 0x7F, codes 0, row
- *     inv_rms NaN.
+ *     inv_rms NaN.  The tensor scale the library derives from a tensor is
+ *     g = RN_fp32(a / 2688) with a the largest finite |x| (2688 = 448 * 6,
+ *     so the tensor's largest block gets the largest E4M3 scale), and
+ *     g = 1 when no finite element is nonzero.
  *   - Backward (straight-through estimator, [MXN] section 2, "Gradientes":
  *     RMSNorm's gradient logic reused, nothing saved but the normaliser):
  *     the cast is treated as the identity and RMSNorm's backward runs with
@@ -492,6 +495,21 @@ int oracle_rmsnorm_mxfp8_rows(const uint16_t *x, int64_t T, int64_t H, float eps
 static double e4m3_code_value(uint8_t c)
 {
     return e4m3_value(c & 0x7F);
+}
+
+/* NVFP4 tensor scale of n bf16 values (see the header comment): the
+ * largest finite magnitude a, then a / 2688 rounded once to fp32.  The
+ * quotient is formed in double and rounded to float: for one division of
+ * two floats that equals the correctly rounded float quotient (double
+ * carries more than 2 * 24 + 2 bits). */
+float oracle_nvfp4_tensor_scale(const uint16_t *x, int64_t n)
+{
+    double a = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double v = fabs((double)bf16_bits_to_float(x[i]));
+        if (isfinite(v) && v > a) a = v;
+    }
+    return a > 0.0 ? (float)(a / 2688.0) : 1.0f;
 }
 
 /* NVFP4 forward of T rows (see the header comment): codes [T, H/2] (element

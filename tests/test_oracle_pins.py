@@ -948,3 +948,23 @@ def test_bf16_rounding_overflows_to_inf_like_torch(oracle_mod):
     got = oracle_mod.float_to_bf16(f)
     assert np.array_equal(got, want)
     assert got[np.where(u == 0x7F7F8000)[0][0]] == 0x7F80 and got[np.where(u == 0x7F7F7FFF)[0][0]] == 0x7F7F
+
+
+def test_nvfp4_tensor_scale(oracle_mod):
+    """g = RN_fp32(a / 2688), a the largest finite |x|: exact powers of two
+    where a = 2688 * 2^j, numpy's IEEE fp32 division elsewhere, Inf and NaN
+    ignored, 1.0 for a tensor with no finite nonzero element."""
+    for j in (-20, -3, 0, 5, 60):
+        x = np.zeros(64, np.float32)
+        x[7] = -2688.0 * 2.0 ** j
+        assert oracle_mod.nvfp4_tensor_scale(synth.f32_to_bf16_bits(x)) == 2.0 ** j
+    rng = np.random.default_rng(45)
+    for _ in range(200):
+        xb = synth.make_random_rows(1, 300, seed=int(rng.integers(1 << 30)), scale=float(np.exp(rng.normal(0, 8))))[0]
+        a = np.abs(synth.bf16_bits_to_f32(xb)).max()
+        assert oracle_mod.nvfp4_tensor_scale(xb) == float(np.float32(a) / np.float32(2688.0))
+    xb = synth.f32_to_bf16_bits(np.array([3.0, -5.0, 0.5], np.float32))
+    xb = np.concatenate([xb, np.array([0x7F80, 0xFFC1, 0xFF80], np.uint16)])
+    assert oracle_mod.nvfp4_tensor_scale(xb) == float(np.float32(5.0) / np.float32(2688.0))
+    assert oracle_mod.nvfp4_tensor_scale(np.array([0, 0x8000, 0x7FC0], np.uint16)) == 1.0
+    assert oracle_mod.nvfp4_tensor_scale(np.array([0x0001], np.uint16)) == float(np.float32(2.0 ** -133) / np.float32(2688.0))
