@@ -7,13 +7,20 @@
 // the gradient, and RMSNorm's backward runs with the forward's estimate
 // rho~ (inv_rms) in place of 1/RMS:
 //     dx = rho~ dy - rho~^3 x (1/H) sum_j dy_j x_j.
+// The kernel evaluates the same expression in the grouping
+//     xh_j = rho~ x_j,   m = (1/H) sum_j dy_j xh_j,   dx_j = rho~ (dy_j - xh_j m),
+// whose fp32 intermediates all sit near the scale of the normalised row:
+// rho~^3 alone leaves the fp32 range once rho~ passes 2^42 (rows whose
+// largest element is below about 2^-34, an all-zero row's rho~ = 2^127)
+// or drops below 2^-43.  With xh = rho~ x of order one, every intermediate
+// is in range while the products dy_j xh_j and their row sum are.
 //
 // One warp per row (grid-stride).  Pass 1 streams x and dy from HBM and
-// reduces sum dy*x in fp32 (pairwise within a lane's VEC values, serial
+// reduces sum dy*xh in fp32 (pairwise within a lane's VEC values, serial
 // over chunks, 5-level warp tree).  Pass 2 re-reads the row -- it is still
-// in L2, a few microseconds later -- and writes dx = fma(-k, x, rho~ dy)
-// with k = rho~^3 * dot / H, two lanes per instruction (f32x2), packed to
-// bf16x2.  HBM traffic per row: 2H (x) + 2H (dy) + 2H (dx) + 4 bytes.
+// in L2, a few microseconds later -- and writes dx = rho~ * fma(-xh, m, dy),
+// two lanes per instruction (f32x2), packed to bf16x2.  HBM traffic per
+// row: 2H (x) + 2H (dy) + 2H (dx) + 4 bytes.
 #include "launch.h"
 #include "mx_row.cuh"
 
@@ -34,13 +41,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// sum over the lane's VEC elements of dy * RN(r x), each product rounded
+// to fp32, pairwise.
 template <int VEC>
-__device__ __forceinline__ float lane_dot(const uint32_t (&wx)[VEC / 2], const uint32_t (&wg)[VEC / 2]) {
+__device__ __forceinline__ float lane_dot(const uint32_t (&wx)[VEC / 2], const uint32_t (&wg)[VEC / 2],
+                                          unsigned long long r2) {
   float s[VEC];
 #pragma unroll
   for (int i = 0; i < VEC / 2; ++i) {
-    s[2 * i] = __fmul_rn(bf16lo(wx[i]), bf16lo(wg[i]));
-    s[2 * i + 1] = __fmul_rn(bf16hi(wx[i]), bf16hi(wg[i]));
+    const unsigned long long xh = f2_mul(r2, f2_pack(bf16lo(wx[i]), bf16hi(wx[i])));
+    f2_unpack(f2_mul(xh, f2_pack(bf16lo(wg[i]), bf16hi(wg[i]))), s[2 * i], s[2 * i + 1]);
   }
 #pragma unroll
   for (int width = VEC / 2; width >= 1; width >>= 1)
@@ -49,17 +59,19 @@ __device__ __forceinline__ float lane_dot(const uint32_t (&wx)[VEC / 2], const u
   return s[0];
 }
 
+// dx = RN(r * RN(dy - RN(r x) m)) for the lane's VEC elements (the fma
+// rounds once), packed to bf16.
 template <int VEC>
 __device__ __forceinline__ void store_dx(uint16_t* dst, const uint32_t (&wx)[VEC / 2],
                                          const uint32_t (&wg)[VEC / 2], unsigned long long r2,
-                                         unsigned long long nk2) {
+                                         unsigned long long nm2) {
   uint32_t o[VEC / 2];
 #pragma unroll
   for (int i = 0; i < VEC / 2; ++i) {
     const unsigned long long g = f2_pack(bf16lo(wg[i]), bf16hi(wg[i]));
-    const unsigned long long xv = f2_pack(bf16lo(wx[i]), bf16hi(wx[i]));
+    const unsigned long long xh = f2_mul(r2, f2_pack(bf16lo(wx[i]), bf16hi(wx[i])));
     float lo, hi;
-    f2_unpack(f2_fma(nk2, xv, f2_mul(r2, g)), lo, hi);
+    f2_unpack(f2_mul(r2, f2_fma(xh, nm2, g)), lo, hi);
     o[i] = pack_bf16x2(lo, hi);
   }
 #pragma unroll
@@ -82,6 +94,8 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     const uint16_t* xr = x + row * (int64_t)H;
     const uint16_t* gr = dy + row * (int64_t)H;
     uint16_t* dr = dx + row * (int64_t)H;
+    const float r = inv_rms[row];
+    const unsigned long long r2 = f2_pack(r, r);
     float dot = 0.0f;
     for (int c0 = 0; c0 < nchunk; c0 += B) {
       uint32_t wx[B][VEC / 2], wg[B][VEC / 2];
@@ -97,13 +111,12 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
         }
       }
 #pragma unroll
-      for (int b = 0; b < B; ++b) dot = __fadd_rn(dot, lane_dot<VEC>(wx[b], wg[b]));
+      for (int b = 0; b < B; ++b) dot = __fadd_rn(dot, lane_dot<VEC>(wx[b], wg[b], r2));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dot = __fadd_rn(dot, __shfl_xor_sync(0xFFFFFFFFu, dot, off));
-    const float r = inv_rms[row];
-    const float k = __fmul_rn(__fmul_rn(__fmul_rn(r, r), r), __fdiv_rn(dot, (float)H));
-    const unsigned long long r2 = f2_pack(r, r), nk2 = f2_pack(-k, -k);
+    const float m = __fdiv_rn(dot, (float)H);
+    const unsigned long long nm2 = f2_pack(-m, -m);
     for (int c0 = 0; c0 < nchunk; c0 += B) {
       uint32_t wx[B][VEC / 2], wg[B][VEC / 2];
 #pragma unroll
@@ -117,7 +130,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
 #pragma unroll
       for (int b = 0; b < B; ++b) {
         const int e0 = (c0 + b) * CE + lane * VEC;
-        if (c0 + b < nchunk && e0 < H) store_dx<VEC>(dr + e0, wx[b], wg[b], r2, nk2);
+        if (c0 + b < nchunk && e0 < H) store_dx<VEC>(dr + e0, wx[b], wg[b], r2, nm2);
       }
     }
   }
