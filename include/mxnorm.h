@@ -48,8 +48,8 @@
  *   inv_rms  float  [T]             4-byte aligned
  * No call allocates device memory (the one buffer the library holds is the
  * static workspace of rmsnorm_mxfp8_ref_fwd_static_ws, below); the library
- * keeps no state between calls except a per-thread error string and
- * per-device launch-shape and workspace-address caches, and it never
+ * keeps no state between calls except a per-thread error string and a
+ * per-device cache of launch shapes, and it never
  * synchronises: work is queued on `stream` (a cudaStream_t; NULL is
  * the legacy default stream) and the call returns.  Outputs are fully
  * written when the stream reaches the kernel's end; after an error return
@@ -186,8 +186,10 @@ int mxnorm_linear_fwd(const void* x_codes, const uint8_t* x_scales, const float*
 
 /* Two-pass baseline: the unfused pipeline MXNorm replaces ("MXNorm ...",
  * Resumen tecnico, section 1: RMSNorm and the MXFP8 cast as separate
- * operations).  Kernel 1: inv = 1/sqrt(mean(x^2) + eps) (fp32 sum, fp64
- * root), y = bf16(fp32(x * inv)) written to y_workspace, inv to inv_rms.
+ * operations).  Kernel 1: inv = 1/sqrt(mean(x^2) + eps) in fp32 (the sum
+ * of squares, the mean and + eps each rounded to fp32, then a correctly
+ * rounded fp32 reciprocal square root), y = bf16(fp32(x * inv)) written to
+ * y_workspace, inv to inv_rms.
  * Kernel 2: MXFP8 E4M3 cast of y (same rules as above) into codes/scales.
  * y_workspace: bf16 [T, H], 16-byte aligned, caller-owned; it holds y on
  * return.  No gain (gamma = 1). */
@@ -213,6 +215,26 @@ int rmsnorm_mxfp8_ref_fwd(const void* x, int64_t T, int64_t H, float eps, void* 
  * MXNORM_ERR_INVALID_ARG). */
 int mxnorm_quant_fwd_nvfp4(const void* x, int64_t T, int64_t H, int p, float tensor_scale, void* codes,
                            uint8_t* scales, float* inv_rms, void* stream);
+
+/* As mxnorm_quant_fwd_nvfp4, with the tensor scale read from device memory
+ * at the start of the kernel (tensor_scale: one fp32, 4-byte aligned), so a
+ * scale derived on the device -- mxnorm_nvfp4_tensor_scale on the same
+ * stream -- reaches the cast without a host round trip.  The value must be
+ * finite and > 0: otherwise the outputs are unspecified and bit 2 of
+ * mxnorm_device_errors is set.  Other errors and stream semantics as
+ * mxnorm_quant_fwd_nvfp4. */
+int mxnorm_quant_fwd_nvfp4_dev(const void* x, int64_t T, int64_t H, int p, const float* tensor_scale,
+                               void* codes, uint8_t* scales, float* inv_rms, void* stream);
+
+/* The NVFP4 tensor scale of n bf16 values, on the device: with a the
+ * largest finite |x| (Inf and NaN elements are skipped; the cast marks
+ * their blocks anyway), *tensor_scale = RN_fp32(a / 2688) -- 2688 = 448 * 6,
+ * so the tensor's largest block gets the largest E4M3 block scale -- or 1
+ * when no finite element is nonzero.  Always a finite positive fp32.
+ * tensor_scale: device pointer to one fp32 (4-byte aligned), written on
+ * `stream` (zeroed, reduced into, then converted: the call queues three
+ * operations and returns). */
+int mxnorm_nvfp4_tensor_scale(const void* x, int64_t n, float* tensor_scale, void* stream);
 
 /* max |x| over n bf16 values, written as an fp32 to the device pointer amax
  * (NaN if any x is NaN).  Zeroes *amax first on the same stream. */
@@ -248,9 +270,11 @@ int mxnorm_bwd_ste(const void* x, const void* dy, const float* inv_rms, int64_t 
  *     the GPU (other streams, other host threads) race on it and must be
  *     serialised by the caller.  The array keeps the last call's y; nothing
  *     in it needs to start at zero.
- *   - The first call on each device, with that device current, looks up the
- *     array's device address once (cudaGetSymbolAddress); make that first
- *     call before any stream capture.
+ *   - Every call looks up the array's address in the current device's
+ *     context (cudaGetSymbolAddress, host-side, no device work), so it
+ *     stays valid after cudaDeviceReset or under another context; the first
+ *     call on a device may load the library's module into that context:
+ *     make it before any stream capture.
  * Arguments, outputs and other errors as rmsnorm_mxfp8_ref_fwd without
  * y_workspace. */
 #define MXNORM_STATIC_WS_BYTES (32u << 20)
@@ -266,10 +290,27 @@ const char* mxnorm_last_error(void);
 /* MXNORM_ABI_VERSION of the loaded library. */
 int mxnorm_abi_version(void);
 
+/* Failure-detection drill for the tiled variant's bounded waits: the
+ * MXFP8, p = 2 pass of mxnorm_quant_fwd_ex with MXNORM_VARIANT_TILED_TMA,
+ * except that the producer never issues the copy of one 8-row tile
+ * (withheld_tile, in [0, ceil(T/8))) and every pipeline wait gives up after
+ * wait_limit_ns (in [1e5, 1e9] ns) instead of one second.  The consumers of
+ * that tile, and the producer waiting for them to release its stage, give
+ * up after the limit; the kernel ends, bit 0 of mxnorm_device_errors is
+ * set, and the call's outputs are invalid (the withheld tile's rows, and
+ * later rows of the CTA that owned it, are never written).  No copy is left
+ * in flight and nothing faults: a caller can check its failure handling end
+ * to end, then clear the word and carry on with the same context.
+ * Arguments and other errors as mxnorm_quant_fwd_ex (T == 0 is
+ * MXNORM_ERR_INVALID_ARG here). */
+int mxnorm_tiled_wait_drill(const void* x, int64_t T, int64_t H, void* codes, uint8_t* scales, float* inv_rms,
+                            int64_t withheld_tile, int64_t wait_limit_ns, void* stream);
+
 /* Device-side error word of the current device, or'ed by kernels whose
  * bounded waits gave up (bit 0: a shared-memory pipeline wait of the tiled
- * variant timed out; bit 1: one of mxnorm_linear_fwd; the outputs of the
- * affected call are then invalid).
+ * variant timed out; bit 1: one of mxnorm_linear_fwd; bit 2: the device
+ * tensor scale given to mxnorm_quant_fwd_nvfp4_dev was not a finite
+ * positive float; the outputs of the affected call are then invalid).
  * Synchronous: copies the word to *flags (and zeroes it when clear != 0).
  * Call after the work in question has completed. */
 int mxnorm_device_errors(uint32_t* flags, int clear);

@@ -20,7 +20,7 @@ __all__ = [
     "FMT", "VARIANT", "MXNormError", "MXNormLibraryMissing", "lib", "library_path",
     "mxnorm_quant_fwd", "quant_fwd", "quant_fwd_host", "rmsnorm_mxfp8_ref_fwd", "device_errors",
     "code_bytes", "bwd_ste", "quant_fwd_nvfp4", "absmax", "nvfp4_tensor_scale", "quant_fwd_mma", "mx_cast",
-    "linear_fwd", "mma_scale_bytes",
+    "linear_fwd", "mma_scale_bytes", "tiled_wait_drill",
 ]
 
 FMT = {"mxfp8": 0, "mxfp4": 1, "mxfp4_h16": 2, "mxfp8_h16": 3, "mxfp4_h32": 4, "mxfp8_h32": 5}
@@ -72,6 +72,10 @@ def lib() -> ctypes.CDLL:
     L.mxnorm_quant_fwd_nvfp4.restype = i32
     L.mxnorm_absmax_bf16.argtypes = [vp, i64, vp, vp]
     L.mxnorm_absmax_bf16.restype = i32
+    L.mxnorm_quant_fwd_nvfp4_dev.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp, vp]
+    L.mxnorm_quant_fwd_nvfp4_dev.restype = i32
+    L.mxnorm_nvfp4_tensor_scale.argtypes = [vp, i64, vp, vp]
+    L.mxnorm_nvfp4_tensor_scale.restype = i32
     L.mxnorm_bwd_ste.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     L.mxnorm_mma_scale_bytes.argtypes = [i64, i64]
     L.mxnorm_mma_scale_bytes.restype = i64
@@ -84,6 +88,8 @@ def lib() -> ctypes.CDLL:
     L.mxnorm_linear_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]
     L.mxnorm_linear_fwd.restype = i32
     L.mxnorm_bwd_ste.restype = i32
+    L.mxnorm_tiled_wait_drill.argtypes = [vp, i64, i64, vp, vp, vp, i64, i64, vp]
+    L.mxnorm_tiled_wait_drill.restype = i32
     L.mxnorm_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     L.mxnorm_device_errors.restype = i32
     _lib = L
@@ -198,26 +204,36 @@ def absmax(x, stream=None):
     return out
 
 
-def nvfp4_tensor_scale(x) -> float:
-    """The usual NVFP4 tensor scale amax(x) / (448 * 6) (fp32; 1.0 for an
-    all-zero tensor).  Synchronises to read amax."""
-    import numpy as np
-    a = np.float32(absmax(x).item())
-    return float(a / np.float32(2688.0)) if a > 0 else 1.0
+def nvfp4_tensor_scale(x, stream=None):
+    """The NVFP4 tensor scale of a contiguous bf16 CUDA tensor, derived by
+    the library on the device (mxnorm_nvfp4_tensor_scale: the largest finite
+    |x| / (448 * 6), rounded to fp32; 1 when there is none but zero).
+    Returns a 1-element float32 CUDA tensor; asynchronous."""
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous bfloat16 CUDA tensor")
+    out = torch.empty((1,), dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        _check(lib().mxnorm_nvfp4_tensor_scale(x.data_ptr(), x.numel(), out.data_ptr(),
+                                               _stream_ptr(x.device, stream)))
+    return out
 
 
 def quant_fwd_nvfp4(x, p: int = 2, tensor_scale=None, out=None, stream=None):
     """MXNorm over the NVFP4 cast of a contiguous bf16 CUDA tensor [..., H]
     (H % 16 == 0).  Returns (codes uint8 [..., H/2], scales uint8 [..., H/16]
-    UE4M3, inv_rms float32 [...]).  tensor_scale defaults to
-    nvfp4_tensor_scale(x)."""
+    UE4M3, inv_rms float32 [...]).  tensor_scale: a float (passed by value),
+    a 1-element float32 CUDA tensor (read by the kernel on the device), or
+    None for nvfp4_tensor_scale(x) derived on the device (no host round
+    trip either way but the float)."""
     import torch
     if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
         raise ValueError("x must be a contiguous bfloat16 CUDA tensor")
     H = x.shape[-1]
     T = x.numel() // H if H else 0
     lead = tuple(x.shape[:-1])
-    g = nvfp4_tensor_scale(x) if tensor_scale is None else float(tensor_scale)
+    if tensor_scale is None:
+        tensor_scale = nvfp4_tensor_scale(x, stream)
     if out is None:
         out = (torch.empty(lead + (H // 2,), dtype=torch.uint8, device=x.device),
                torch.empty(lead + (H // 16,), dtype=torch.uint8, device=x.device),
@@ -227,8 +243,14 @@ def quant_fwd_nvfp4(x, p: int = 2, tensor_scale=None, out=None, stream=None):
     _require(scales, "scales", x.device, min_numel=T * (H // 16), byte_elems=True)
     _require(inv, "inv_rms", x.device, torch.float32, T)
     with torch.cuda.device(x.device):
-        _check(lib().mxnorm_quant_fwd_nvfp4(x.data_ptr(), T, H, int(p), g, codes.data_ptr(), scales.data_ptr(),
-                                            inv.data_ptr(), _stream_ptr(x.device, stream)))
+        if isinstance(tensor_scale, torch.Tensor):
+            _require(tensor_scale, "tensor_scale", x.device, torch.float32, 1)
+            _check(lib().mxnorm_quant_fwd_nvfp4_dev(x.data_ptr(), T, H, int(p), tensor_scale.data_ptr(),
+                                                    codes.data_ptr(), scales.data_ptr(), inv.data_ptr(),
+                                                    _stream_ptr(x.device, stream)))
+        else:
+            _check(lib().mxnorm_quant_fwd_nvfp4(x.data_ptr(), T, H, int(p), float(tensor_scale), codes.data_ptr(),
+                                                scales.data_ptr(), inv.data_ptr(), _stream_ptr(x.device, stream)))
     return codes, scales, inv
 
 
@@ -353,9 +375,35 @@ def bwd_ste(x, dy, inv_rms, out=None, stream=None):
     return dx
 
 
+def tiled_wait_drill(x, withheld_tile: int = 0, wait_limit_ns: int = 2_000_000, out=None, stream=None):
+    """Failure-detection drill (mxnorm_tiled_wait_drill): the tiled MXFP8
+    pass with one tile's copy withheld, so that its bounded waits expire
+    after wait_limit_ns and bit 0 of device_errors() gets set.  Returns the
+    (invalid) outputs (codes, scales, inv_rms)."""
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous bfloat16 CUDA tensor")
+    H = x.shape[-1]
+    T = x.numel() // H if H else 0
+    if out is None:
+        out = (torch.empty((T, H), dtype=torch.uint8, device=x.device),
+               torch.empty((T, H // 32), dtype=torch.uint8, device=x.device),
+               torch.empty((T,), dtype=torch.float32, device=x.device))
+    codes, scales, inv = out
+    _require(codes, "codes", x.device, min_numel=T * H, byte_elems=True)
+    _require(scales, "scales", x.device, min_numel=T * (H // 32), byte_elems=True)
+    _require(inv, "inv_rms", x.device, torch.float32, T)
+    with torch.cuda.device(x.device):
+        _check(lib().mxnorm_tiled_wait_drill(x.data_ptr(), T, H, codes.data_ptr(), scales.data_ptr(),
+                                             inv.data_ptr(), int(withheld_tile), int(wait_limit_ns),
+                                             _stream_ptr(x.device, stream)))
+    return codes, scales, inv
+
+
 def device_errors(clear: bool = True) -> int:
     """The device error flags: bit 0, a bounded wait of the tiled kernel
-    timed out; bit 1, a pipeline wait of the GEMM timed out."""
+    timed out; bit 1, a pipeline wait of the GEMM timed out; bit 2, a device
+    NVFP4 tensor scale was not a finite positive float."""
     v = ctypes.c_uint32(0)
     _check(lib().mxnorm_device_errors(ctypes.byref(v), int(clear)))
     return v.value

@@ -38,6 +38,8 @@ int cuda_fail(cudaError_t err, const char* what) {
   return fail(MXNORM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
 }
 
+}  // namespace
+
 int check_common(const void* x, int64_t T, int64_t H, const void* codes, const void* scales,
                  const void* inv_rms) {
   if (T < 0) return fail(MXNORM_ERR_INVALID_ARG, "T = %lld < 0", (long long)T);
@@ -52,8 +54,6 @@ int check_common(const void* x, int64_t T, int64_t H, const void* codes, const v
   if (!aligned(inv_rms, 4)) return fail(MXNORM_ERR_MISALIGNED, "inv_rms is not 4-byte aligned");
   return MXNORM_OK;
 }
-
-}  // namespace
 
 void set_last_error(const char* msg) { g_last_error = msg; }
 
@@ -100,9 +100,30 @@ int mxnorm_quant_fwd_ex(const void* x, int64_t T, int64_t H, int p, int fmt, voi
   WarpRowArgs a{x, T, H, p, fmt, codes, scales, inv_rms};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool use_tiled = variant == MXNORM_VARIANT_TILED_TMA;
-  cudaError_t err = use_tiled ? launch_mxnorm_tiled(TiledArgs{a, nullptr}, s)
-                              : launch_mxnorm_warp_row(a, s);
+  cudaError_t err = use_tiled ? launch_mxnorm_tiled(TiledArgs{a}, s) : launch_mxnorm_warp_row(a, s);
   if (err != cudaSuccess) return cuda_fail(err, "mxnorm_quant_fwd launch");
+  return MXNORM_OK;
+}
+
+int mxnorm_tiled_wait_drill(const void* x, int64_t T, int64_t H, void* codes, uint8_t* scales, float* inv_rms,
+                            int64_t withheld_tile, int64_t wait_limit_ns, void* stream) {
+  g_last_error.clear();
+  int st = check_common(x, T, H, codes, scales, inv_rms);
+  if (st != MXNORM_OK) return st;
+  if (T == 0) return fail(MXNORM_ERR_INVALID_ARG, "the drill needs at least one row");
+  if (!tiled_supported(H, MXNORM_FMT_MXFP8_E4M3))
+    return fail(MXNORM_ERR_UNSUPPORTED, "tiled variant does not support H = %lld", (long long)H);
+  const int64_t ntiles = (T + 7) / 8;
+  if (withheld_tile < 0 || withheld_tile >= ntiles)
+    return fail(MXNORM_ERR_INVALID_ARG, "withheld_tile = %lld is not in [0, %lld)", (long long)withheld_tile,
+                (long long)ntiles);
+  if (wait_limit_ns < 100000 || wait_limit_ns > 1000000000)
+    return fail(MXNORM_ERR_INVALID_ARG, "wait_limit_ns = %lld is not in [1e5, 1e9]", (long long)wait_limit_ns);
+  TiledArgs t{WarpRowArgs{x, T, H, 2, MXNORM_FMT_MXFP8_E4M3, codes, scales, inv_rms}};
+  t.wait_limit_ns = (unsigned long long)wait_limit_ns;
+  t.withheld_tile = withheld_tile;
+  cudaError_t err = launch_mxnorm_tiled(t, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "mxnorm_tiled_wait_drill launch");
   return MXNORM_OK;
 }
 
@@ -260,6 +281,39 @@ int mxnorm_quant_fwd_nvfp4(const void* x, int64_t T, int64_t H, int p, float ten
   return MXNORM_OK;
 }
 
+int mxnorm_quant_fwd_nvfp4_dev(const void* x, int64_t T, int64_t H, int p, const float* tensor_scale,
+                               void* codes, uint8_t* scales, float* inv_rms, void* stream) {
+  g_last_error.clear();
+  if (p != 1 && p != 2) return fail(MXNORM_ERR_INVALID_ARG, "p = %d is not 1 or 2", p);
+  if (T < 0) return fail(MXNORM_ERR_INVALID_ARG, "T = %lld < 0", (long long)T);
+  if (H <= 0 || H % 16 != 0)
+    return fail(MXNORM_ERR_INVALID_ARG, "H = %lld is not a positive multiple of 16", (long long)H);
+  if (H > MXNORM_MAX_H)
+    return fail(MXNORM_ERR_UNSUPPORTED, "H = %lld exceeds MXNORM_MAX_H = %d", (long long)H, MXNORM_MAX_H);
+  if (T == 0) return MXNORM_OK;
+  if (!x || !tensor_scale || !codes || !scales || !inv_rms)
+    return fail(MXNORM_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(x, 16) || !aligned(codes, 16)) return fail(MXNORM_ERR_MISALIGNED, "x and codes need 16-byte alignment");
+  if (!aligned(inv_rms, 4) || !aligned(tensor_scale, 4))
+    return fail(MXNORM_ERR_MISALIGNED, "inv_rms and tensor_scale need 4-byte alignment");
+  Nvfp4Args a{x, T, H, p, 1.0f, codes, scales, inv_rms};
+  a.g_dev = tensor_scale;
+  cudaError_t err = launch_nvfp4(a, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "mxnorm_quant_fwd_nvfp4_dev launch");
+  return MXNORM_OK;
+}
+
+int mxnorm_nvfp4_tensor_scale(const void* x, int64_t n, float* tensor_scale, void* stream) {
+  g_last_error.clear();
+  if (n < 0) return fail(MXNORM_ERR_INVALID_ARG, "n < 0");
+  if (!tensor_scale || (n > 0 && !x)) return fail(MXNORM_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned(tensor_scale, 4) || !aligned(x, 2))
+    return fail(MXNORM_ERR_MISALIGNED, "tensor_scale needs 4-byte, x 2-byte alignment");
+  cudaError_t err = launch_nvfp4_tensor_scale(x, n, tensor_scale, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "mxnorm_nvfp4_tensor_scale launch");
+  return MXNORM_OK;
+}
+
 int mxnorm_absmax_bf16(const void* x, int64_t n, float* amax, void* stream) {
   g_last_error.clear();
   if (n < 0) return fail(MXNORM_ERR_INVALID_ARG, "n < 0");
@@ -287,11 +341,12 @@ int mxnorm_abi_version(void) { return MXNORM_ABI_VERSION; }
 
 int mxnorm_device_errors(uint32_t* flags, int clear) {
   if (!flags) return fail(MXNORM_ERR_INVALID_ARG, "NULL flags");
-  uint32_t tiled = 0, linear = 0;
+  uint32_t tiled = 0, linear = 0, nvfp4 = 0;
   cudaError_t err = read_device_error_word(&tiled, clear != 0);
   if (err == cudaSuccess) err = read_linear_error_word(&linear, clear != 0);
+  if (err == cudaSuccess) err = read_nvfp4_error_word(&nvfp4, clear != 0);
   if (err != cudaSuccess) return cuda_fail(err, "reading the device error words");
-  *flags = (tiled & 1u) | ((linear & 1u) << 1);
+  *flags = (tiled & 1u) | ((linear & 1u) << 1) | ((nvfp4 & 1u) << 2);
   return MXNORM_OK;
 }
 

@@ -42,10 +42,11 @@ struct Nvfp4Args {
   int64_t T;
   int64_t H;
   int p;
-  float g;             // fp32 tensor scale (> 0, finite)
+  float g;             // fp32 tensor scale (> 0, finite), used when g_dev is null
   void* codes;         // u8 [T, H/2]
   uint8_t* scales;     // UE4M3 [T, H/16]
   float* inv_rms;      // f32 [T]
+  const float* g_dev = nullptr;  // device word holding the tensor scale, or null
 };
 
 struct LinearArgs {
@@ -73,7 +74,8 @@ struct GainCastArgs {
 
 struct TiledArgs {
   WarpRowArgs base;
-  unsigned int* error_flag;  // device word set when a bounded wait gives up
+  unsigned long long wait_limit_ns = 1000000000ull;  // limit of the pipeline waits
+  int64_t withheld_tile = -1;  // failure-detection drill: a tile whose copy is never issued
 };
 
 // Grid size for a grid-stride kernel: enough CTAs to fill every SM at the
@@ -92,9 +94,17 @@ cudaError_t launch_mxfp8_linear(const LinearArgs& a, cudaStream_t s);
 cudaError_t launch_mx_cast_gain(const GainCastArgs& a, cudaStream_t s);
 cudaError_t read_linear_error_word(uint32_t* out, bool clear);
 cudaError_t launch_absmax_bf16(const void* x, int64_t n, float* amax, cudaStream_t s);
+cudaError_t launch_nvfp4_tensor_scale(const void* x, int64_t n, float* g, cudaStream_t s);
+cudaError_t read_nvfp4_error_word(uint32_t* out, bool clear);
 
 // Replace the calling thread's message returned by mxnorm_last_error().
 void set_last_error(const char* msg);
+
+// Checks shared by the entry points that take (x, T, H, codes, scales,
+// inv_rms): sizes, NULL pointers (T > 0) and alignment; returns an
+// mxnorm_status and sets the thread's message on failure.
+int check_common(const void* x, int64_t T, int64_t H, const void* codes, const void* scales,
+                 const void* inv_rms);
 
 // Copy (and optionally zero) the device error word that bounded waits set.
 cudaError_t read_device_error_word(uint32_t* out, bool clear);

@@ -18,10 +18,21 @@
 // One warp per row (grid-stride), lane l of chunk c owning block
 // 32 c + l: a 32-byte load, no block shuffles.  Rows stream through a ring
 // of AHEAD chunk buffers as in the MXNorm warp-row kernel.
+//
+// The tensor scale comes from the caller, as an fp32 argument or as a
+// device word (read by every thread at kernel start, so that a scale
+// derived on the device needs no host round trip).  The library derives it
+// from a tensor as g = RN(a / 2688), a the largest finite |x| (448 * 6:
+// the tensor's largest block then gets the largest E4M3 scale), or 1 when
+// no finite element is nonzero; a device word that is not a finite
+// positive float sets bit 0 of g_nvfp4_error_word.
 #include "launch.h"
 #include "mx_row.cuh"
 
 namespace mxnorm {
+
+__device__ unsigned int g_nvfp4_error_word = 0u;
+
 namespace {
 
 constexpr int kWarps = 8;
@@ -77,11 +88,17 @@ __device__ __forceinline__ float nvfp4_inv(unsigned long long s, bool bad, int K
 
 template <int NCHUNK, int AHEAD, bool EXACT, bool LOAD32, int MINB>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
-    nvfp4_row_kernel(const uint16_t* __restrict__ x, int64_t T, int H, int p, float g,
-                     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ inv_rms) {
+    nvfp4_row_kernel(const uint16_t* __restrict__ x, int64_t T, int H, int p, float g_arg,
+                     const float* __restrict__ g_dev, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                     float* __restrict__ inv_rms) {
   static_assert(NCHUNK == 0 || NCHUNK % AHEAD == 0, "the ring must tile the row");
   constexpr int CE = 512;
   const int lane = threadIdx.x & 31;
+  float g = g_arg;
+  if (g_dev != nullptr) {
+    g = *g_dev;
+    if (!(g > 0.0f && g <= 3.4028235e38f) && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&g_nvfp4_error_word, 1u);
+  }
   const int Hc = (EXACT && NCHUNK > 0) ? NCHUNK * CE : H;
   const int K = Hc / 16;
   const float sixg = __fmul_rn(6.0f, g);
@@ -158,7 +175,7 @@ cudaError_t launch_one(const Nvfp4Args& a, cudaStream_t s) {
   auto kern = exact ? nvfp4_row_kernel<NCHUNK, AHEAD, true, LOAD32, MINB>
                     : nvfp4_row_kernel<NCHUNK, AHEAD, false, LOAD32, MINB>;
   const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kWarps * 32, (a.T + kWarps - 1) / kWarps);
-  kern<<<grid, kWarps * 32, 0, s>>>(static_cast<const uint16_t*>(a.x), a.T, (int)a.H, a.p, a.g,
+  kern<<<grid, kWarps * 32, 0, s>>>(static_cast<const uint16_t*>(a.x), a.T, (int)a.H, a.p, a.g, a.g_dev,
                                     static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms);
   return cudaGetLastError();
 }
@@ -179,12 +196,16 @@ cudaError_t launch_h(const Nvfp4Args& a, cudaStream_t s) {
 }
 
 // max |x| over n bf16 values into *out (non-negative floats order like
-// their bits, NaN above Inf): per-CTA tree, then one atomicMax per CTA.
+// their bits, NaN above Inf; FINITE skips Inf and NaN): per-CTA tree, then
+// one atomicMax per CTA.
+template <bool FINITE>
 __global__ void __launch_bounds__(256) absmax_bf16_kernel(const uint16_t* __restrict__ x, int64_t n,
                                                           unsigned int* __restrict__ out) {
   unsigned int m = 0u;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-    m = max(m, ((uint32_t)x[i] << 16) & 0x7FFFFFFFu);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t b = ((uint32_t)x[i] << 16) & 0x7FFFFFFFu;
+    if (!FINITE || b < 0x7F800000u) m = max(m, b);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
   __shared__ unsigned int red[8];
@@ -196,6 +217,23 @@ __global__ void __launch_bounds__(256) absmax_bf16_kernel(const uint16_t* __rest
   }
 }
 
+// In place: the largest finite magnitude's bits at *g become the tensor
+// scale RN(a / 2688), or 1 when a = 0.
+__global__ void nvfp4_scale_from_amax_kernel(float* g) {
+  const float a = __uint_as_float(*reinterpret_cast<const unsigned int*>(g));
+  *g = a > 0.0f ? __fdiv_rn(a, 2688.0f) : 1.0f;
+}
+
+template <bool FINITE>
+cudaError_t launch_absmax(const void* x, int64_t n, float* amax, cudaStream_t s) {
+  cudaError_t err = cudaMemsetAsync(amax, 0, sizeof(float), s);
+  if (err != cudaSuccess || n == 0) return err;
+  auto kern = absmax_bf16_kernel<FINITE>;
+  const int grid = persistent_grid(reinterpret_cast<const void*>(kern), 256, (n + 255) / 256);
+  kern<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), n, reinterpret_cast<unsigned int*>(amax));
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_nvfp4(const Nvfp4Args& a, cudaStream_t s) {
@@ -204,12 +242,26 @@ cudaError_t launch_nvfp4(const Nvfp4Args& a, cudaStream_t s) {
 }
 
 cudaError_t launch_absmax_bf16(const void* x, int64_t n, float* amax, cudaStream_t s) {
-  cudaError_t err = cudaMemsetAsync(amax, 0, sizeof(float), s);
-  if (err != cudaSuccess || n == 0) return err;
-  auto kern = absmax_bf16_kernel;
-  const int grid = persistent_grid(reinterpret_cast<const void*>(kern), 256, (n + 255) / 256);
-  kern<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), n, reinterpret_cast<unsigned int*>(amax));
+  return launch_absmax<false>(x, n, amax, s);
+}
+
+cudaError_t launch_nvfp4_tensor_scale(const void* x, int64_t n, float* g, cudaStream_t s) {
+  cudaError_t err = launch_absmax<true>(x, n, g, s);
+  if (err != cudaSuccess) return err;
+  nvfp4_scale_from_amax_kernel<<<1, 1, 0, s>>>(g);
   return cudaGetLastError();
+}
+
+cudaError_t read_nvfp4_error_word(uint32_t* out, bool clear) {
+  unsigned int v = 0;
+  cudaError_t err = cudaMemcpyFromSymbol(&v, g_nvfp4_error_word, sizeof v);
+  if (err != cudaSuccess) return err;
+  *out = v;
+  if (clear) {
+    const unsigned int zero = 0;
+    err = cudaMemcpyToSymbol(g_nvfp4_error_word, &zero, sizeof zero);
+  }
+  return err;
 }
 
 }  // namespace mxnorm

@@ -11,11 +11,16 @@
 // shared-memory loads, then arriving on the stage's "empty" mbarrier.
 // The producer refills a stage after all eight consumers released it.
 //
-// Every wait is bounded by a wall-clock deadline (%globaltimer, about one
-// second): on expiry the waiter sets bit 0 of the device error word
-// (read with mxnorm_device_errors) and stops; before the CTA exits, the
-// producer waits (again bounded) for every copy it issued, so no bulk copy
-// can still be writing into shared memory of a retired CTA.
+// Every wait is bounded by a wall-clock deadline (%globaltimer, one second
+// unless the launch asks for less): on expiry the waiter sets bit 0 of the
+// device error word (read with mxnorm_device_errors) and stops; before the
+// CTA exits, the producer waits (bounded by one second) for every copy it
+// issued, so no bulk copy can still be writing into shared memory of a
+// retired CTA.  The failure-detection drill (mxnorm_tiled_wait_drill) runs
+// the same kernel with a short limit and one tile whose copy the producer
+// never issues: the consumers of that tile, and the producer waiting for
+// them to release its stage, give up after the limit; the drain skips the
+// withheld copy, since none is in flight.
 //
 // Method as in the warp-row kernel ("MXNorm: Reusing MXFP block scales ...",
 // Resumen tecnico, 2. Metodologia, Fundamentos Teoricos / Implementacion).
@@ -32,7 +37,7 @@ constexpr int kConsumers = 8;                 // consumer warps = rows per tile
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kSmemBudget = 200 * 1024;       // ring bytes per CTA
 constexpr int kMaxStages = 8;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s: the normal limit, and the drain's
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -69,13 +74,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0u;
 }
 
-// Bounded wait for the phase with the given parity; false on timeout (and
-// the device error word then has bit 0 set).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Bounded wait for the phase with the given parity; false after limit_ns
+// (and the device error word then has bit 0 set).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(&g_device_error_word, 1u);
       return false;
     }
@@ -111,7 +117,8 @@ __device__ __forceinline__ void lds_lane(uint32_t saddr, uint32_t (&w)[VEC / 2])
 template <int FMT, int VEC, int NCHUNK>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_tiled_kernel(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
-                    uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p, int stages) {
+                    uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p, int stages,
+                    unsigned long long wait_ns, int64_t withheld_tile) {
   using Tr = FmtTraits<FMT>;
   extern __shared__ __align__(128) unsigned char smem[];
   // layout: [full mbarriers x kMaxStages][empty x kMaxStages] then the ring
@@ -138,21 +145,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol = evict_first_policy();
-      int64_t issued = 0;
+      int64_t issued = 0, withheld_at = -1;
       bool ok = true;
       for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++issued) {
         const int s = (int)(issued % stages);
         const uint32_t use = (uint32_t)(issued / stages);
-        if (use > 0) ok = mbar_wait_bounded(empty0 + 8 * s, (use - 1) & 1u);
+        if (use > 0) ok = mbar_wait_bounded(empty0 + 8 * s, (use - 1) & 1u, wait_ns);
         if (!ok) break;
+        if (tile == withheld_tile) {  // drill: this stage's phase never completes
+          withheld_at = issued;
+          continue;
+        }
         const int64_t r0 = tile * kConsumers;
         const int64_t nrows = min((int64_t)kConsumers, T - r0);
         const uint32_t bytes = (uint32_t)(nrows * row_bytes);
         mbar_arrive_expect_tx(full0 + 8 * s, bytes);
         bulk_g2s(ring0 + (uint32_t)(s * stage_bytes), x + r0 * H, bytes, full0 + 8 * s, pol);
       }
-      // Drain: the last use of every stage must have landed before exit.
+      // Drain: the last use of every stage must have landed before exit
+      // (a withheld copy was never issued, so there is nothing to wait for).
       for (int64_t i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
+        if (i == withheld_at) continue;
         const int s = (int)(i % stages);
         (void)mbar_wait_bounded(full0 + 8 * s, (uint32_t)(i / stages) & 1u);
       }
@@ -165,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
     const int s = (int)(i % stages);
     const uint32_t use = (uint32_t)(i / stages);
-    if (!mbar_wait_bounded(full0 + 8 * s, use & 1u)) break;
+    if (!mbar_wait_bounded(full0 + 8 * s, use & 1u, wait_ns)) break;
     const int64_t row = tile * kConsumers + r;
     if (row < T) {
       const uint32_t srow = ring0 + (uint32_t)(s * stage_bytes + r * row_bytes);
@@ -201,7 +214,8 @@ cudaError_t launch_one(const TiledArgs& t, cudaStream_t s) {
   const int64_t ntiles = (a.T + kConsumers - 1) / kConsumers;
   const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kThreads, ntiles, smem);
   kern<<<grid, kThreads, smem, s>>>(static_cast<const uint16_t*>(a.x), a.T, (int)a.H,
-                                    static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms, a.p, stages);
+                                    static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms, a.p, stages,
+                                    t.wait_limit_ns, t.withheld_tile);
   return cudaGetLastError();
 }
 

@@ -20,11 +20,11 @@
 // kernel of the same call, so nothing has to start at zero.
 //
 // Device address: in host code `g_static_ws` names a host-side shadow, not
-// device memory.  The first call on each device (with that device current)
-// resolves the array's device address once with cudaGetSymbolAddress and
-// caches it; that first call should come before any stream capture.
-#include <mutex>
-
+// device memory.  Every call looks up the array's address in the current
+// device's context with cudaGetSymbolAddress (a host-side lookup; no device
+// work), so the address stays right after cudaDeviceReset or under another
+// context on the same device.  The first call on a device may load the
+// module into that context: make it before any stream capture.
 #include "launch.h"
 #include "mx_device.cuh"
 #include "mxnorm.h"
@@ -33,33 +33,12 @@ namespace mxnorm {
 namespace {
 
 constexpr size_t kStaticWsBytes = MXNORM_STATIC_WS_BYTES;
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
-
-std::mutex g_ws_mu;
-void* g_ws_ptr[kMaxDevices] = {};
 
 int static_fail(int status, const char* msg) {
   set_last_error(msg);
   return status;
-}
-
-// Device address of the workspace on the current device (resolved once).
-cudaError_t workspace_on_current_device(void** out) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_ws_mu);
-  if (g_ws_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_static_ws);
-    if (err != cudaSuccess) return err;
-    g_ws_ptr[dev] = p;
-  }
-  *out = g_ws_ptr[dev];
-  return cudaSuccess;
 }
 
 }  // namespace
@@ -71,19 +50,15 @@ extern "C" int rmsnorm_mxfp8_ref_fwd_static_ws(const void* x, int64_t T, int64_t
                                                uint8_t* codes, uint8_t* scales, float* inv_rms,
                                                void* stream) {
   set_last_error("");
-  if (T < 0 || H <= 0 || H % kBlock != 0)
-    return static_fail(MXNORM_ERR_INVALID_ARG, "T must be >= 0 and H a positive multiple of 32");
   if (!(eps >= 0.0f)) return static_fail(MXNORM_ERR_INVALID_ARG, "eps must be >= 0");
-  if (H > MXNORM_MAX_H || T > (int64_t)(kStaticWsBytes / 2) / H)
+  const int st = check_common(x, T, H, codes, scales, inv_rms);
+  if (st != MXNORM_OK) return st;
+  if (T > (int64_t)(kStaticWsBytes / 2) / H)
     return static_fail(MXNORM_ERR_UNSUPPORTED,
                        "T * H exceeds the static workspace (MXNORM_STATIC_WS_BYTES / 2 bf16 elements)");
   if (T == 0) return MXNORM_OK;
-  if (!x || !codes || !scales || !inv_rms) return static_fail(MXNORM_ERR_INVALID_ARG, "NULL pointer argument");
-  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(codes) & 15) ||
-      (reinterpret_cast<uintptr_t>(inv_rms) & 3))
-    return static_fail(MXNORM_ERR_MISALIGNED, "x and codes need 16-byte, inv_rms 4-byte alignment");
   void* ws = nullptr;
-  cudaError_t err = workspace_on_current_device(&ws);
+  cudaError_t err = cudaGetSymbolAddress(&ws, g_static_ws);
   if (err != cudaSuccess) return static_fail(MXNORM_ERR_CUDA, cudaGetErrorString(err));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   err = launch_rmsnorm_bf16(RmsNormArgs{x, T, H, eps, ws, inv_rms}, s);

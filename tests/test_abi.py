@@ -97,6 +97,61 @@ def test_nvfp4_validation(L):
     assert q(FAKE, 8, 48, 2, 1.0, FAKE + 8, FAKE, FAKE, None) == 3
     assert L.mxnorm_absmax_bf16(FAKE, -1, FAKE, None) == 1
     assert L.mxnorm_absmax_bf16(FAKE, 8, None, None) == 1
+    d = L.mxnorm_quant_fwd_nvfp4_dev
+    assert d(FAKE, 0, 4096, 2, FAKE, FAKE, FAKE, FAKE, None) == 0
+    assert d(FAKE, 8, 4096, 3, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert d(FAKE, 8, 4096, 2, None, FAKE, FAKE, FAKE, None) == 1
+    assert d(FAKE, 8, 24, 2, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert d(FAKE, 8, 48, 2, FAKE + 2, FAKE, FAKE, FAKE, None) == 3
+    assert d(FAKE, 8, 48, 2, FAKE, FAKE + 8, FAKE, FAKE, None) == 3
+    assert d(FAKE, 8, (1 << 20) + 16, 2, FAKE, FAKE, FAKE, FAKE, None) == 2
+    ts = L.mxnorm_nvfp4_tensor_scale
+    assert ts(FAKE, -1, FAKE, None) == 1
+    assert ts(FAKE, 8, None, None) == 1
+    assert ts(None, 8, FAKE, None) == 1
+    assert ts(FAKE, 8, FAKE + 2, None) == 3
+
+
+def test_static_workspace_validation(L):
+    """The allocation-free baseline entry checks its arguments as
+    rmsnorm_mxfp8_ref_fwd does (same checks, same statuses), then the size
+    of its built-in workspace: T * H above MXNORM_STATIC_WS_BYTES / 2."""
+    f = L.rmsnorm_mxfp8_ref_fwd_static_ws
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    H = 4096
+    limit_rows = (32 << 20) // 2 // H
+    assert f(FAKE, limit_rows + 1, H, 1e-5, FAKE, FAKE, FAKE, None) == 2
+    assert b"static workspace" in L.mxnorm_last_error()
+    assert f(FAKE, 0, H, 1e-5, FAKE, FAKE, FAKE, None) == 0
+    assert f(FAKE, -1, H, 1e-5, FAKE, FAKE, FAKE, None) == 1
+    assert f(FAKE, 8, 100, 1e-5, FAKE, FAKE, FAKE, None) == 1
+    assert f(FAKE, 8, (1 << 20) + 32, 1e-5, FAKE, FAKE, FAKE, None) == 2
+    assert b"MXNORM_MAX_H" in L.mxnorm_last_error()
+    assert f(FAKE, 8, H, -1.0, FAKE, FAKE, FAKE, None) == 1
+    assert f(FAKE, 8, H, float("nan"), FAKE, FAKE, FAKE, None) == 1
+    assert f(None, 8, H, 1e-5, FAKE, FAKE, FAKE, None) == 1
+    assert f(FAKE, 8, H, 1e-5, FAKE, None, FAKE, None) == 1
+    assert f(FAKE + 8, 8, H, 1e-5, FAKE, FAKE, FAKE, None) == 3
+    assert f(FAKE, 8, H, 1e-5, FAKE + 4, FAKE, FAKE, None) == 3
+    assert f(FAKE, 8, H, 1e-5, FAKE, FAKE, FAKE + 2, None) == 3
+
+
+def test_wait_drill_validation(L):
+    """The drill entry point refuses what it cannot run before any launch:
+    an empty input, a tile outside the input, a wait limit outside
+    [1e5, 1e9] ns, and the usual shape, pointer and alignment errors."""
+    w = L.mxnorm_tiled_wait_drill
+    assert w(FAKE, 0, 4096, FAKE, FAKE, FAKE, 0, 2000000, None) == 1
+    assert w(FAKE, 16, 4096, FAKE, FAKE, FAKE, 2, 2000000, None) == 1
+    assert w(FAKE, 16, 4096, FAKE, FAKE, FAKE, -1, 2000000, None) == 1
+    assert w(FAKE, 16, 4096, FAKE, FAKE, FAKE, 0, 99999, None) == 1
+    assert w(FAKE, 16, 4096, FAKE, FAKE, FAKE, 0, 1000000001, None) == 1
+    assert w(FAKE, 16, 100, FAKE, FAKE, FAKE, 0, 2000000, None) == 1
+    assert w(FAKE, 16, 8192, FAKE, FAKE, FAKE, 0, 2000000, None) == 2   # the tiled ring holds H <= 6400
+    assert w(None, 16, 4096, FAKE, FAKE, FAKE, 0, 2000000, None) == 1
+    assert w(FAKE + 8, 16, 4096, FAKE, FAKE, FAKE, 0, 2000000, None) == 3
 
 
 def test_linear_and_layout_validation(L):

@@ -176,7 +176,7 @@ def check_gain_cast(wb, g, c, layout, w_dev=None, rows=None):
     torch.cuda.synchronize()
     N, K = wb.shape
     rows = np.arange(N) if rows is None else np.asarray(rows)
-    oc, os_ = oracle.mx_cast_gain(np.ascontiguousarray(wb[rows]), g, c)
+    oc, os_ = oracle.rows_in_threads(lambda a: oracle.mx_cast_gain(a, g, c), np.ascontiguousarray(wb[rows]))
     got_c = codes.cpu().numpy()
     np.testing.assert_array_equal(got_c[rows], oc)
     got_s = scales.cpu().numpy()
@@ -233,14 +233,15 @@ def test_gain_cast_16_byte_aligned_weight():
     check_gain_cast(wb, gains(K, 8), 1.0, "mma", w_dev=w)
 
 
-def test_gain_cast_llama3_8b_gate_up_sampled():
-    """The Llama-3-8B fused gate/up weight (28672 x 4096) in the MMA layout,
-    the oracle on sampled rows (both ends and random rows of many strips)."""
+@pytest.mark.parametrize("layout", ["mma", "row_major"])
+def test_gain_cast_llama3_8b_gate_up_every_row(layout):
+    """The Llama-3-8B fused gate/up weight (28672 x 4096), the launch the
+    benchmark times: every row against the oracle, codes and scales
+    bit-exact ("MXNorm ...", 2. Metodologia, Implementacion: the norm's gain
+    folded into the next layer's weight)."""
     N, K = 28672, 4096
     wb = synth.make_random_rows(N, K, seed=12, scale=0.02)
-    rng = np.random.default_rng(12)
-    rows = np.unique(np.concatenate([np.arange(4), np.arange(N - 4, N), rng.integers(0, N, 56)]))
-    check_gain_cast(wb, gains(K, 12), 1.0, "mma", rows=rows)
+    check_gain_cast(wb, gains(K, 12), 1.0, layout)
 
 
 def test_linear_with_gain_folded_weight():
@@ -291,3 +292,63 @@ def test_linear_matches_cublaslt_mxfp8():
     a, b = ours.double(), ref.double()
     assert ((a - b).abs() <= 2.0 ** -7 * b.abs() + 2.0 ** -12 * b.abs().max()).all()
     print(f"bit-equal fraction vs cuBLASLt: {(ours.view(torch.int16) == ref.view(torch.int16)).double().mean().item():.6f}")
+
+
+def test_weight_cast_and_quant_layout_outputs_stay_in_bounds():
+    """Guard bytes around the gain-folded cast's codes and scales (both
+    layouts) and around the fused pass's MMA-layout scales survive, on
+    ragged row counts (not multiples of 8 or 128)."""
+    gd = 4096
+    for N, K in ((77, 4096), (301, 1152), (1, 128)):
+        wb = synth.make_random_rows(N, K, seed=N + K, scale=0.05)
+        gam = gains(K, N)
+        for layout, lid in (("row_major", 0), ("mma", 1)):
+            nsc = N * K // 32 if lid == 0 else mx.mma_scale_bytes(N, K)
+            codes = torch.full((N * K + 2 * gd,), 0xA5, dtype=torch.uint8, device="cuda")
+            scales = torch.full((nsc + 2 * gd,), 0x5A, dtype=torch.uint8, device="cuda")
+            gt, wt = torch.from_numpy(gam).cuda(), dev(wb)
+            st = mx.lib().mx_cast_gain_fwd(wt.data_ptr(), N, K, gt.data_ptr(), 1.3,
+                                           codes[gd:].data_ptr(), scales[gd:].data_ptr(), lid, None)
+            torch.cuda.synchronize()
+            assert st == 0
+            assert (codes[:gd] == 0xA5).all() and (codes[gd + N * K:] == 0xA5).all(), (N, K, layout)
+            assert (scales[:gd] == 0x5A).all() and (scales[gd + nsc:] == 0x5A).all(), (N, K, layout)
+            oc, os_ = oracle.mx_cast_gain(wb, gam, 1.3)
+            assert np.array_equal(codes[gd:gd + N * K].cpu().numpy().reshape(N, K), oc)
+    for T, H in ((300, 768), (5, 4096)):
+        xb = synth.make_random_rows(T, H, seed=T, scale=2.0)
+        nsc = mx.mma_scale_bytes(T, H)
+        codes = torch.full((T * H + 2 * gd,), 0xA5, dtype=torch.uint8, device="cuda")
+        scales = torch.full((nsc + 2 * gd,), 0x5A, dtype=torch.uint8, device="cuda")
+        inv = torch.full((T + 2 * gd,), 7.0, dtype=torch.float32, device="cuda")
+        xt = dev(xb)
+        st = mx.lib().mxnorm_quant_fwd_layout(xt.data_ptr(), T, H, 2, 0, codes[gd:].data_ptr(),
+                                              scales[gd:].data_ptr(), inv[gd:].data_ptr(), 1, None)
+        torch.cuda.synchronize()
+        assert st == 0
+        assert (codes[:gd] == 0xA5).all() and (codes[gd + T * H:] == 0xA5).all()
+        assert (scales[:gd] == 0x5A).all() and (scales[gd + nsc:] == 0x5A).all()
+        assert (inv[:gd] == 7.0).all() and (inv[gd + T:] == 7.0).all()
+        oc, os_, oi = oracle.mxnorm_quant(xb, 2, "mxfp8")
+        got = scales[gd:gd + nsc].cpu().numpy()
+        mask = mma_mask(T, H // 32)
+        assert np.array_equal(got[mask], to_mma_layout(os_)[mask])
+
+
+def test_linear_out_stays_in_bounds():
+    """Guard elements around the GEMM's output survive, with T off the
+    128-row tile (a ragged last tile) and several 256-column tiles."""
+    gd = 4096
+    T, K, N = 300, 512, 768
+    xb = synth.make_random_rows(T, K, seed=31, scale=2.0)
+    wb = synth.make_random_rows(N, K, seed=32, scale=0.05)
+    xc, xs, inv = mx.quant_fwd_mma(dev(xb))
+    wc, ws = mx.mx_cast(dev(wb), "mma")
+    buf = torch.full((T * N + 2 * gd,), 5.0, dtype=torch.bfloat16, device="cuda")
+    out = mx.linear_fwd(xc, xs, inv, wc, ws, out=buf[gd:gd + T * N])
+    torch.cuda.synchronize()
+    assert (buf[:gd] == 5.0).all() and (buf[-gd:] == 5.0).all()
+    assert mx.device_errors() == 0
+    ref = mx.linear_fwd(xc, xs, inv, wc, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(T, N), ref)

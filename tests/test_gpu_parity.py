@@ -147,40 +147,41 @@ def test_llama3_125m_all_elements(p, variant):
     assert_parity(workload_input("llama3_125m_16384x768"), p, "mxfp8", variant)
 
 
-def sample_rows(T, n=192, seed=0):
-    rng = np.random.default_rng(seed)
-    return np.unique(np.concatenate([np.arange(32), np.arange(T - 32, T), rng.integers(0, T, n)]))
+def oracle_all_rows(xb, p, fmt):
+    """The oracle over every row, rows split across the host cores."""
+    return oracle.rows_in_threads(lambda a: oracle.mxnorm_quant(a, p, fmt), xb)
 
 
 @pytest.mark.parametrize("name,fmt,ps", [
     ("llama3_1b_32768x2048", "mxfp8", (2,)),
     ("llama3_8b_65536x4096", "mxfp8", (1, 2)),
+    ("llama3_8b_65536x4096", "mxfp4", (2,)),
     ("llama3_8b_mxfp4_h16_65536x4096", "mxfp4_h16", (2,)),
     ("llama3_8b_mxfp4_h16_65536x4096", "mxfp4_h32", (2,)),
     ("llama3_8b_mxfp4_h16_65536x4096", "mxfp8_h16", (2,)),
     ("llama3_8b_mxfp4_h16_65536x4096", "mxfp8_h32", (2,)),
-    ("llama3_8b_65536x4096", "mxfp4", (2,)),
 ])
-def test_full_size_workloads_sampled_rows(name, fmt, ps):
-    """Full-size inputs in the launch configuration the benchmark times
-    (auto variant and both explicit variants); the oracle checks sampled rows
-    bit-exactly, and on every row the variants agree and the invariants hold
-    (scale codes in range, no NaN codes, inv_rms consistent with the scales)."""
+def test_full_size_workloads_every_row(name, fmt, ps):
+    """Full-size inputs in the launch configuration the benchmark times,
+    compared with the oracle element by element on every row: codes and
+    E8M0 scales bit-exact, inv_rms within 1e-6 relative -- the estimator of
+    "MXNorm ...", 2. Metodologia, Fundamentos Teoricos, on the block scales
+    of the cast.  The auto variant is checked against the oracle; the
+    explicit warp-row and tiled variants must equal it bit for bit."""
     xb = workload_input(name)
     T, H = xb.shape
-    rows = sample_rows(T)
     for p in ps:
-        c, s, i = assert_parity(xb, p, fmt, "auto", rows)
+        c, s, i = run(xb, p, fmt, "auto")
+        oc, os_, oi = oracle_all_rows(xb, p, fmt)
+        bad = np.nonzero((c != oc).any(1))[0]
+        assert bad.size == 0, f"codes differ in {bad.size} of {T} rows, first row {bad[:1]}"
+        bad = np.nonzero((s != os_).any(1))[0]
+        assert bad.size == 0, f"scales differ in {bad.size} of {T} rows, first row {bad[:1]}"
+        assert_inv_close(i, oi)
+        del oc, os_, oi
         for v in variants_for(H):
             c2, s2, i2 = run(xb, p, fmt, v)
             assert np.array_equal(c2, c) and np.array_equal(s2, s) and np.array_equal(i2, i), v
-        assert s.min() >= 0 and s.max() <= 254
-        if fmt.startswith("mxfp8"):
-            assert not ((c & 0x7F) == 0x7F).any()
-        e = s.astype(np.float64) - 127
-        mean = np.exp2(p * e).mean(1)
-        est = 1.0 / (mean if p == 1 else np.sqrt(mean))
-        assert np.abs(i.astype(np.float64) / est - 1).max() <= INV_RTOL
 
 
 # --------------------------------------------------------- edge cases
@@ -335,25 +336,25 @@ def baseline_inv_rtol(H):
     return (L + 2) * 2.0 ** -25 + 2 * 2.0 ** -24
 
 
-@pytest.mark.parametrize("name,rows", [("tiny_64x256", None), ("llama3_1b_32768x2048", 1024),
-                                       ("llama3_8b_65536x4096", 512)])
-def test_rmsnorm_mxfp8_baseline(name, rows):
-    xb = workload_input(name, rows)
+@pytest.mark.parametrize("name", ["tiny_64x256", "llama3_1b_32768x2048", "llama3_8b_65536x4096"])
+def test_rmsnorm_mxfp8_baseline(name):
+    """The two-pass baseline on every row of the workload."""
+    xb = workload_input(name)
     T, H = xb.shape
     y, c, s, i = mx.rmsnorm_mxfp8_ref_fwd(dev(xb), eps=1e-5)
     torch.cuda.synchronize()
     yb = y.view(torch.int16).cpu().numpy().view(np.uint16)
     c, s, i = c.cpu().numpy(), s.cpu().numpy(), i.cpu().numpy()
-    oy, oc, os_, oi = oracle.rmsnorm_mxfp8(xb, 1e-5)
+    oy, oc, os_, oi = oracle.rows_in_threads(lambda a: oracle.rmsnorm_mxfp8(a, 1e-5), xb)
     assert_inv_close(i, oi, rtol=baseline_inv_rtol(H))
     # y is x * inv in fp32 rounded to bf16, with the GPU's own inv
     want_y = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(xb) * i[:, None])
     assert np.array_equal(yb, want_y)
     # within one bf16 ulp of the oracle's y
-    a, b = synth.bf16_bits_to_f32(yb).astype(np.float64), synth.bf16_bits_to_f32(oy).astype(np.float64)
+    a, b = synth.bf16_bits_to_f32(yb), synth.bf16_bits_to_f32(oy)  # differences of bf16 values: exact in fp32
     assert (np.abs(a - b) <= np.abs(b) * 2.0 ** -7 + 1e-38).all()
     # stage 2 is the MXFP8 cast of the GPU's y, bit-exact
-    rc, rs = oracle.mx_cast(yb, "mxfp8")
+    rc, rs = oracle.rows_in_threads(lambda a: oracle.mx_cast(a, "mxfp8"), yb)
     assert np.array_equal(c, rc) and np.array_equal(s, rs)
 
 
