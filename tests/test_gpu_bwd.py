@@ -176,3 +176,18 @@ def test_bwd_extreme_rows(H, p, dy_scale):
     assert inv[4] < 2.0 ** -50 and inv[0] > 2.0 ** 90
     # the all-zero row scales dy by 2^127 exactly: Inf in bf16 beyond 2 |dy|
     check_bwd(xb, gb, inv, min_equal=0.98)
+
+
+def test_bwd_outputs_stay_in_bounds():
+    """Guard elements around dx survive the call, on ragged shapes (the
+    generic-H path, one partial chunk, the 4096 fast path)."""
+    g = 4096
+    for T, H in ((13, 800), (3, 32), (9, 4096)):
+        xb = synth.make_random_rows(T, H, seed=T + H, scale=2.0)
+        gb = synth.make_random_rows(T, H, seed=T * H)
+        _, _, inv = oracle.mxnorm_quant(xb, 2, "mxfp8")
+        buf = torch.full((T * H + 2 * g,), 3.0, dtype=torch.bfloat16, device="cuda")
+        dx = mx.bwd_ste(dev_bf16(xb), dev_bf16(gb), torch.from_numpy(inv).cuda(), out=buf[g:g + T * H])
+        torch.cuda.synchronize()
+        assert (buf[:g] == 3.0).all() and (buf[-g:] == 3.0).all(), (T, H)
+        compare_bwd(dx.view(torch.int16).cpu().numpy().view(np.uint16).reshape(T, H), xb, gb, inv)

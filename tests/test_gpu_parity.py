@@ -234,10 +234,11 @@ def test_special_rows(H, fmt):
 def tiny_block_rows(H, seed):
     """Rows whose 32-element blocks sit at bf16 exponent fields from 60 down
     to 0 (2^-67 .. subnormal), one level per block, with random mantissas
-    and signs; the last rows mix a normal value into tiny blocks.  After the
-    H16 butterfly these blocks straddle max |z| = 2^-100, where the kernel
-    switches between folding the quarter into the exponent and applying it
-    explicitly."""
+    and signs; the last rows mix a normal value into tiny blocks.  The
+    rotations' fp32 sums and their final scale (1/4 or 1/sqrt(32)) then
+    produce subnormal fp32 values, which must round exactly as the oracle's
+    butterfly does (no flush to zero), and blocks whose amax is subnormal
+    get the clamped scale exponent -127."""
     rng = np.random.default_rng(seed)
     K = H // 32
     fields = np.linspace(60, 0, K).round().astype(np.int64)
