@@ -233,8 +233,10 @@ def run_gpu(args):
     abytes = algorithmic_bytes(T, H, "mxfp8")
     achieved = abytes / (mean_launch * 1e-3) / 1e9
 
-    # ---- secondary measurements (same stream, fewer steps)
-    sec_steps = max(20, min(args.steps, 300))
+    # ---- secondary measurements (same stream): at least 200 launches each
+    # whatever --steps is, so that short headline runs still time the
+    # smaller legs over many launches (each is well under a millisecond)
+    sec_steps = max(200, min(args.steps, 500))
     extra = {}
 
     def gbs(nbytes, ms):
@@ -267,14 +269,17 @@ def run_gpu(args):
                                "bytes_per_row": 6 * H + 4}
     del dy, dxs
 
-    # NVFP4 (16-element blocks, UE4M3 scales, tensor scale from amax / (448*6))
-    g = mx.nvfp4_tensor_scale(xs[0])
+    # NVFP4 (16-element blocks, UE4M3 scales); the tensor scale amax / (448*6)
+    # derived by the library on the device once (both buffers hold the same
+    # rows) and read by the kernel from device memory
+    with torch.cuda.stream(stream):
+        g_dev = mx.nvfp4_tensor_scale(xs[0], stream=stream)
     c4n = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
     s4n = torch.empty((T, H // 16), dtype=torch.uint8, device=dev)
 
     def nvfp4_step(i):
-        st = mx.lib().mxnorm_quant_fwd_nvfp4(xs[i].data_ptr(), T, H, 2, ctypes.c_float(g), c4n.data_ptr(),
-                                             s4n.data_ptr(), outs[i][2].data_ptr(), ctypes.c_void_p(sptr))
+        st = mx.lib().mxnorm_quant_fwd_nvfp4_dev(xs[i].data_ptr(), T, H, 2, g_dev.data_ptr(), c4n.data_ptr(),
+                                                 s4n.data_ptr(), outs[i][2].data_ptr(), ctypes.c_void_p(sptr))
         if st:
             raise RuntimeError(mx.lib().mxnorm_last_error().decode())
 
@@ -337,6 +342,54 @@ def run_gpu(args):
                                             "speedup_of_mxnorm_p2": round(b1 / m1, 3)},
         "l2": "4 rotating 128 MiB input buffers"}
     del x1, c1, s1, i1, y1
+
+    # The Llama-3-125M-shaped workload (16384 x 768, p = 1 and 2): 38 MB per
+    # launch, well inside L2, so twelve input and output sets rotate (458 MB,
+    # over 3x the 129 MB L2): a set was last touched eleven launches (420 MB
+    # of traffic) earlier and streams from HBM again.  Timed per launch with
+    # events, and as a CUDA graph of back-to-back launches (the rate a
+    # caller issuing them in a row sees, launch gaps included).
+    w125 = synth.WORKLOADS["llama3_125m_16384x768"]
+    T2, H2 = w125.T, w125.H
+    x2h = torch.from_numpy(synth.make_activations(w125).view(np.int16)).view(torch.bfloat16)
+    nb2 = 12
+    x2 = [x2h.to(dev) for _ in range(nb2)]
+    o2 = [(torch.empty((T2, H2), dtype=torch.uint8, device=dev),
+           torch.empty((T2, H2 // 32), dtype=torch.uint8, device=dev),
+           torch.empty((T2,), dtype=torch.float32, device=dev)) for _ in range(nb2)]
+    a2 = algorithmic_bytes(T2, H2, "mxfp8")
+    leg125 = extra["llama3_125m_16384x768"] = {
+        "l2": f"{nb2} rotating input+output sets, {round(nb2 * a2 / 2 ** 20)} MiB in all (> 2 x L2)"}
+    for p2 in (1, 2):
+        def s125(i, p2=p2):
+            c, s_, v = o2[i]
+            mx.mxnorm_quant_fwd(x2[i].data_ptr(), T2, H2, p2, 0, c.data_ptr(), s_.data_ptr(), v.data_ptr(), sptr, 0)
+
+        per2, _ = time_launches(torch, stream, s125, max(sec_steps, 4 * nb2 * 10), 2 * nb2, nb2)
+        m2 = statistics.fmean(per2)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(nb2):
+                s125(i)
+        reps = 40
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graph.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        mg = e0.elapsed_time(e1) / (reps * nb2)
+        del graph
+        leg125[f"mxnorm_mxfp8_p{p2}"] = {
+            "ms": round(m2, 5), "GB/s": gbs(a2, m2), "frac": round(gbs(a2, m2) / hbm_peak, 4),
+            "tokens_per_s": round(T2 / (m2 * 1e-3), 1),
+            "graph_back_to_back": {"ms_per_launch": round(mg, 5), "GB/s": gbs(a2, mg),
+                                   "frac": round(gbs(a2, mg) / hbm_peak, 4),
+                                   "tokens_per_s": round(T2 / (mg * 1e-3), 1)}}
+    del x2, o2
 
     if not args.skip_fp4:
         # the rotated formats on the MXFP4+H16 workload's input (same distribution, seed 4)
