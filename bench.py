@@ -9,15 +9,18 @@ scales, fp32 inverse-RMS estimate.  Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
-value      tokens/s over all ranks, inputs resident in HBM, CUDA events on the
-           launching stream around every step; inputs (2 x 512 MiB, rotated)
-           exceed the 129 MB L2, so no flush is needed between steps.
+value      tokens/s over all ranks, inputs resident in HBM: K back-to-back
+           steps on the launching stream between one pair of CUDA events
+           (an event pair around every launch stalls the stream between
+           launches; that figure is reported beside it); inputs (2 x 512 MiB,
+           rotated) exceed the 129 MB L2, so no flush is needed between steps.
 e2e        the same metric through the public API from pinned host buffers:
            the C-ABI call on pinned host memory (zero-copy: the kernel reads x
            and writes codes, scales and inv_rms across the host link), every
            step inside the timed region.
 roofline   HBM-bound: algorithmic bytes per launch (2H + H + H/32 + 4 per row)
-           / mean per-launch time, against the measured HBM copy bandwidth.
+           / mean launch time (timed region / steps, launch gaps included),
+           against the measured HBM copy bandwidth.
 --impl reference   the CPU oracle (oracle/, test infrastructure) timed on a
            bounded sample of the same workload on the host cores.
 """
@@ -154,9 +157,55 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------- GPU timing
-def time_launches(torch, stream, fn, steps: int, warmup: int, nbuf: int):
-    """fn(i) launches one step on `stream` using buffer set i % nbuf; returns
-    (per-launch ms list, region ms)."""
+SLEEP_CYCLES = 200_000  # about 0.1 ms of device sleep queued before a timed region
+
+
+def time_region(torch, stream, fn, steps: int, warmup: int, nbuf: int, graph: bool = False) -> float:
+    """ms per launch of `steps` back-to-back launches, fn(i) launching one
+    step on `stream` with buffer set i % nbuf: one CUDA event pair around the
+    whole region (events between launches would stall the stream between
+    them), synchronised on both sides.  A short device sleep queued before
+    the start event lets the host enqueue ahead of the GPU, so the region
+    holds no host gaps.  graph=True captures the launches in a CUDA graph
+    and replays it, for launches shorter than the host's enqueue time."""
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            fn(i % nbuf)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if graph:
+        per_graph = nbuf * max(1, -(-16 // nbuf))  # at least 16 launches per replay
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(per_graph):
+                fn(i % nbuf)
+        reps = max(1, -(-steps // per_graph))
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(SLEEP_CYCLES)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        del g
+        return e0.elapsed_time(e1) / (reps * per_graph)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(SLEEP_CYCLES)
+        e0.record(stream)
+        for i in range(steps):
+            fn(i % nbuf)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def time_each(torch, stream, fn, steps: int, warmup: int, nbuf: int):
+    """Per-launch ms with an event pair around every launch (each pair adds
+    a few microseconds of stream stalls: reported beside the back-to-back
+    figure, not as the kernel's rate)."""
     with torch.cuda.stream(stream):
         for i in range(warmup):
             fn(i % nbuf)
@@ -168,9 +217,7 @@ def time_launches(torch, stream, fn, steps: int, warmup: int, nbuf: int):
             fn(i % nbuf)
             ev[i][1].record(stream)
     torch.cuda.synchronize()
-    per = [a.elapsed_time(b) for a, b in ev]
-    region = ev[0][0].elapsed_time(ev[-1][1])
-    return per, region
+    return [a.elapsed_time(b) for a, b in ev]
 
 
 def run_gpu(args):
@@ -219,14 +266,13 @@ def run_gpu(args):
     torch.cuda.synchronize()
     sampler = ClockSampler(torch.cuda.current_device() if world == 1 else local)
     with sampler:
-        per, region = time_launches(torch, stream, step, args.steps, args.warmup, nbuf)
+        mean_launch = time_region(torch, stream, step, args.steps, args.warmup, nbuf)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    ms_step = region / args.steps
-    mean_launch = statistics.fmean(per)
-    ms_step = shard.max_over_ranks(ms_step, dev)
+    ms_step = shard.max_over_ranks(mean_launch, dev)
     tokens_per_s = world * T / (ms_step * 1e-3)
+    per = time_each(torch, stream, step, max(20, min(args.steps, 200)), 3, nbuf)
 
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
@@ -242,14 +288,11 @@ def run_gpu(args):
     def gbs(nbytes, ms):
         return round(nbytes / (ms * 1e-3) / 1e9, 1)
 
-    per1, _ = time_launches(torch, stream, lambda i: step(i, p=1), sec_steps, 5, nbuf)
-    m = statistics.fmean(per1)
+    m = time_region(torch, stream, lambda i: step(i, p=1), sec_steps, 5, nbuf)
     extra["mxnorm_mxfp8_p1_warp_row"] = {"ms": round(m, 5), "GB/s": gbs(abytes, m), "frac": round(gbs(abytes, m) / hbm_peak, 4)}
-    pert, _ = time_launches(torch, stream, lambda i: step(i, variant=2), sec_steps, 5, nbuf)
-    m = statistics.fmean(pert)
+    m = time_region(torch, stream, lambda i: step(i, variant=2), sec_steps, 5, nbuf)
     extra["mxnorm_mxfp8_p2_tiled_tma"] = {"ms": round(m, 5), "GB/s": gbs(abytes, m), "frac": round(gbs(abytes, m) / hbm_peak, 4)}
-    perw, _ = time_launches(torch, stream, lambda i: step(i, variant=1), sec_steps, 5, nbuf)
-    m = statistics.fmean(perw)
+    m = time_region(torch, stream, lambda i: step(i, variant=1), sec_steps, 5, nbuf)
     extra["mxnorm_mxfp8_p2_warp_row"] = {"ms": round(m, 5), "GB/s": gbs(abytes, m), "frac": round(gbs(abytes, m) / hbm_peak, 4)}
 
     # straight-through backward on the same rows (dy ~ N(0,1), inv from the forward)
@@ -262,8 +305,7 @@ def run_gpu(args):
         if st:
             raise RuntimeError(mx.lib().mxnorm_last_error().decode())
 
-    perbw, _ = time_launches(torch, stream, bwd_step, sec_steps, 5, nbuf)
-    m = statistics.fmean(perbw)
+    m = time_region(torch, stream, bwd_step, sec_steps, 5, nbuf)
     extra["mxnorm_bwd_ste"] = {"ms": round(m, 5), "GB/s": gbs(T * (6 * H + 4), m),
                                "frac": round(gbs(T * (6 * H + 4), m) / hbm_peak, 4),
                                "bytes_per_row": 6 * H + 4}
@@ -283,8 +325,7 @@ def run_gpu(args):
         if st:
             raise RuntimeError(mx.lib().mxnorm_last_error().decode())
 
-    pern, _ = time_launches(torch, stream, nvfp4_step, sec_steps, 5, nbuf)
-    m = statistics.fmean(pern)
+    m = time_region(torch, stream, nvfp4_step, sec_steps, 5, nbuf)
     bn = T * (2 * H + H // 2 + H // 16 + 4)
     extra["mxnorm_nvfp4_p2"] = {"ms": round(m, 5), "GB/s": gbs(bn, m), "frac": round(gbs(bn, m) / hbm_peak, 4),
                                 "bytes_per_row": 2 * H + H // 2 + H // 16 + 4}
@@ -299,8 +340,7 @@ def run_gpu(args):
         if st:
             raise RuntimeError(mx.lib().mxnorm_last_error().decode())
 
-    perb, _ = time_launches(torch, stream, base_step, sec_steps, 5, nbuf)
-    mb = statistics.fmean(perb)
+    mb = time_region(torch, stream, base_step, sec_steps, 5, nbuf)
     extra["two_pass_rmsnorm_mxfp8_baseline"] = {
         "ms": round(mb, 5), "GB/s": gbs(baseline_bytes(T, H), mb),
         "speedup_of_mxnorm_p2": round(mb / mean_launch, 3)}
@@ -330,25 +370,28 @@ def run_gpu(args):
             raise RuntimeError(mx.lib().mxnorm_last_error().decode())
 
     pm1, pb1 = [], []
-    for _ in range(2):  # alternating blocks
-        pm1 += time_launches(torch, stream, mx1_step, sec_steps // 2, 5, nb1)[0]
-        pb1 += time_launches(torch, stream, base1_step, sec_steps // 2, 5, nb1)[0]
+    for _ in range(2):  # alternating blocks, each a CUDA graph of back-to-back launches
+        pm1.append(time_region(torch, stream, mx1_step, sec_steps // 2, 5, nb1, graph=True))
+        pb1.append(time_region(torch, stream, base1_step, sec_steps // 2, 5, nb1, graph=True))
     m1, b1 = statistics.fmean(pm1), statistics.fmean(pb1)
+    e1 = statistics.fmean(time_each(torch, stream, mx1_step, sec_steps // 2, 5, nb1))
     a1 = algorithmic_bytes(T1, H1, "mxfp8")
     extra["llama3_1b_32768x2048"] = {
         "mxnorm_mxfp8_p2": {"ms": round(m1, 5), "GB/s": gbs(a1, m1), "frac": round(gbs(a1, m1) / hbm_peak, 4),
-                            "tokens_per_s": round(T1 / (m1 * 1e-3), 1)},
+                            "tokens_per_s": round(T1 / (m1 * 1e-3), 1),
+                            "event_pair_per_launch_ms": round(e1, 5)},
         "two_pass_rmsnorm_mxfp8_baseline": {"ms": round(b1, 5), "GB/s": gbs(baseline_bytes(T1, H1), b1),
                                             "speedup_of_mxnorm_p2": round(b1 / m1, 3)},
-        "l2": "4 rotating 128 MiB input buffers"}
+        "l2": "4 rotating 128 MiB input buffers",
+        "timing": "CUDA graphs of back-to-back launches, one event pair per timed region"}
     del x1, c1, s1, i1, y1
 
     # The Llama-3-125M-shaped workload (16384 x 768, p = 1 and 2): 38 MB per
     # launch, well inside L2, so twelve input and output sets rotate (458 MB,
     # over 3x the 129 MB L2): a set was last touched eleven launches (420 MB
-    # of traffic) earlier and streams from HBM again.  Timed per launch with
-    # events, and as a CUDA graph of back-to-back launches (the rate a
-    # caller issuing them in a row sees, launch gaps included).
+    # of traffic) earlier and streams from HBM again.  Timed as a CUDA graph
+    # of back-to-back launches (launch gaps included); the mean with an event
+    # pair around every launch is reported beside it.
     w125 = synth.WORKLOADS["llama3_125m_16384x768"]
     T2, H2 = w125.T, w125.H
     x2h = torch.from_numpy(synth.make_activations(w125).view(np.int16)).view(torch.bfloat16)
@@ -365,30 +408,12 @@ def run_gpu(args):
             c, s_, v = o2[i]
             mx.mxnorm_quant_fwd(x2[i].data_ptr(), T2, H2, p2, 0, c.data_ptr(), s_.data_ptr(), v.data_ptr(), sptr, 0)
 
-        per2, _ = time_launches(torch, stream, s125, max(sec_steps, 4 * nb2 * 10), 2 * nb2, nb2)
-        m2 = statistics.fmean(per2)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(nb2):
-                s125(i)
-        reps = 40
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                graph.replay()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(reps):
-                graph.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        mg = e0.elapsed_time(e1) / (reps * nb2)
-        del graph
+        mg = time_region(torch, stream, s125, max(sec_steps, 40 * nb2), 2 * nb2, nb2, graph=True)
+        m2 = statistics.fmean(time_each(torch, stream, s125, 4 * nb2, 2 * nb2, nb2))
         leg125[f"mxnorm_mxfp8_p{p2}"] = {
-            "ms": round(m2, 5), "GB/s": gbs(a2, m2), "frac": round(gbs(a2, m2) / hbm_peak, 4),
-            "tokens_per_s": round(T2 / (m2 * 1e-3), 1),
-            "graph_back_to_back": {"ms_per_launch": round(mg, 5), "GB/s": gbs(a2, mg),
-                                   "frac": round(gbs(a2, mg) / hbm_peak, 4),
-                                   "tokens_per_s": round(T2 / (mg * 1e-3), 1)}}
+            "ms": round(mg, 5), "GB/s": gbs(a2, mg), "frac": round(gbs(a2, mg) / hbm_peak, 4),
+            "tokens_per_s": round(T2 / (mg * 1e-3), 1), "event_pair_per_launch_ms": round(m2, 5)}
+    leg125["timing"] = "CUDA graphs of back-to-back launches, one event pair per timed region"
     del x2, o2
 
     if not args.skip_fp4:
@@ -403,8 +428,7 @@ def run_gpu(args):
                 c, s, v = outs[i]
                 mx.mxnorm_quant_fwd(x4.data_ptr(), T, H, 2, fid, c4.data_ptr(), s.data_ptr(), v.data_ptr(), sptr, 0)
 
-            per4, _ = time_launches(torch, stream, fp4_step, sec_steps, 5, nbuf)
-            m = statistics.fmean(per4)
+            m = time_region(torch, stream, fp4_step, sec_steps, 5, nbuf)
             b4 = algorithmic_bytes(T, H, "mxfp8" if fmt.startswith("mxfp8") else "mxfp4")
             extra[f"mxnorm_{fmt}_p2"] = {"workload": "llama3_8b_mxfp4_h16_65536x4096", "ms": round(m, 5),
                                          "GB/s": gbs(b4, m), "frac": round(gbs(b4, m) / hbm_peak, 4)}
@@ -436,8 +460,8 @@ def run_gpu(args):
 
     perg, perp = [], []
     for _ in range(2):  # alternating blocks
-        perg += time_launches(torch, stream, gain_step, sec_steps // 2, 5, nbuf)[0]
-        perp += time_launches(torch, stream, plain_step, sec_steps // 2, 5, nbuf)[0]
+        perg.append(time_region(torch, stream, gain_step, sec_steps // 2, 5, nbuf))
+        perp.append(time_region(torch, stream, plain_step, sec_steps // 2, 5, nbuf))
     m, mp = statistics.fmean(perg), statistics.fmean(perp)
     bg = Ng * (3 * H + H // 32)
     extra["mx_cast_gain_llama3_8b_gate_up_28672x4096"] = {
@@ -488,17 +512,17 @@ def run_gpu(args):
         torch._scaled_mm(a8, b8.t(), scale_a=xq_scales.view(torch.float8_e8m0fnu),
                          scale_b=w_scales.view(torch.float8_e8m0fnu), out_dtype=torch.bfloat16)
 
-    perq, _ = time_launches(torch, stream, quant_mma_step, sec_steps, 5, nbuf)
+    mq = time_region(torch, stream, quant_mma_step, sec_steps, 5, nbuf)
     lin_steps = max(10, sec_steps // 20)
     perl, perc, cublas_note = [], [], None
     for _ in range(2):
-        perl += time_launches(torch, stream, linear_step, lin_steps, 3, nbuf)[0]
+        perl.append(time_region(torch, stream, linear_step, lin_steps, 3, nbuf))
         if cublas_note is None:
             try:
-                perc += time_launches(torch, stream, cublas_step, lin_steps, 3, nbuf)[0]
+                perc.append(time_region(torch, stream, cublas_step, lin_steps, 3, nbuf))
             except Exception as e:  # no MX support in this torch / cuBLASLt
                 cublas_note = f"unavailable: {type(e).__name__}: {str(e)[:160]}"
-    mq, ml = statistics.fmean(perq), statistics.fmean(perl)
+    ml = statistics.fmean(perl)
     fp8_peak = 2.0 * float(peaks.get("bf16_tflops", 1900.0))
     tflops = 2.0 * T * H * Nw / (ml * 1e-3) / 1e12
     extra["mxnorm_quant_mma_layout_p2"] = {"ms": round(mq, 5), "GB/s": gbs(abytes, mq),
@@ -556,7 +580,10 @@ def run_gpu(args):
                          "frac": round(achieved / hbm_peak, 4), "traffic": profiled_traffic(),
                          "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": abytes,
                          "mean_launch_ms": round(mean_launch, 6),
-                         "median_launch_ms": round(statistics.median(per), 6)},
+                         "timing": "one event pair around the timed region's back-to-back launches; "
+                                   "mean launch = region / steps",
+                         "event_pair_per_launch_ms": {"mean": round(statistics.fmean(per), 6),
+                                                      "median": round(statistics.median(per), 6)}},
             "clocks": sampler.summary(),
             "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
@@ -717,8 +744,7 @@ def run_profile_case(args):
                                            gc.data_ptr(), gs.data_ptr(), 1, ctypes.c_void_p(stream.cuda_stream))
             if st:
                 raise RuntimeError(mx.lib().mxnorm_last_error().decode())
-        per, region = time_launches(torch, stream, fn_gain, args.steps, args.warmup, 1)
-        m = statistics.fmean(per)
+        m = time_region(torch, stream, fn_gain, args.steps, args.warmup, 1)
         print(json.dumps({"profile_only": True, "kernel": "mx_cast_gain_fwd", "N": Ng, "K": H,
                           "mean_launch_ms": round(m, 6),
                           "GB/s": round(Ng * (3 * H + H // 32) / (m * 1e-3) / 1e9, 1)}), flush=True)
@@ -745,8 +771,7 @@ def run_profile_case(args):
             def fn_k(i):
                 mx.quant_fwd_nvfp4(x, 2, tensor_scale=g, out=(c4, s4, inv), stream=stream)
         torch.cuda.synchronize()
-        per, region = time_launches(torch, stream, fn_k, args.steps, args.warmup, 1)
-        m = statistics.fmean(per)
+        m = time_region(torch, stream, fn_k, args.steps, args.warmup, 1)
         print(json.dumps({"profile_only": True, "kernel": kernel, "rows": T, "H": H, "mean_launch_ms": round(m, 6),
                           "GB/s": round(nbytes / (m * 1e-3) / 1e9, 1)}), flush=True)
         return
@@ -763,8 +788,7 @@ def run_profile_case(args):
 
         def fn_lin(i):
             mx.linear_fwd(xc, xs, xinv, w_codes, w_scales, out=out, stream=stream)
-        per, region = time_launches(torch, stream, fn_lin, args.steps, args.warmup, 1)
-        m = statistics.fmean(per)
+        m = time_region(torch, stream, fn_lin, args.steps, args.warmup, 1)
         print(json.dumps({"profile_only": True, "kernel": "mxnorm_linear_fwd", "T": T, "K": H, "N": Nw,
                           "mean_launch_ms": round(m, 6),
                           "TFLOP/s": round(2.0 * T * H * Nw / (m * 1e-3) / 1e12, 1),
@@ -783,9 +807,8 @@ def run_profile_case(args):
             mx.quant_fwd(x, 2, args.profile_fmt, args.profile_variant, out=(codes, scales, inv), stream=stream)
     scales = torch.empty((T, H // 32), dtype=torch.uint8, device="cuda")
     inv = torch.empty((T,), dtype=torch.float32, device="cuda")
-    per, region = time_launches(torch, stream, fn, args.steps, args.warmup, 1)
+    m = time_region(torch, stream, fn, args.steps, args.warmup, 1)
     nbytes = baseline_bytes(T, H) if args.profile_baseline else algorithmic_bytes(T, H, args.profile_fmt)
-    m = statistics.fmean(per)
     print(json.dumps({"profile_only": True, "workload": name, "rows": T, "variant": args.profile_variant,
                       "baseline": args.profile_baseline, "mean_launch_ms": round(m, 6),
                       "GB/s": round(nbytes / (m * 1e-3) / 1e9, 1)}), flush=True)
@@ -818,8 +841,7 @@ def run_shape_sweep(args):
 
         def fn(i):
             mx.quant_fwd(xs[i], 2, "mxfp8", out=outs[i], stream=stream)
-        per, _ = time_launches(torch, stream, fn, args.steps, args.warmup, 2)
-        m = statistics.fmean(per)
+        m = time_region(torch, stream, fn, args.steps, args.warmup, 2)
         g_s = algorithmic_bytes(T, H, "mxfp8") / (m * 1e-3) / 1e9
         res[str(H)] = {"T": T, "ms": round(m, 5), "GB/s": round(g_s, 1), "frac": round(g_s / hbm_peak, 4)}
         del xs, outs
