@@ -78,6 +78,27 @@ struct TiledArgs {
   int64_t withheld_tile = -1;  // failure-detection drill: a tile whose copy is never issued
 };
 
+// Launch a kernel with programmatic stream serialisation: it may be
+// scheduled while the previous kernel on the stream finishes, and waits in
+// pdl_enter() (mx_device.cuh) for that kernel's completion before touching
+// memory.  Grids launched this way fit in one wave (persistent_grid), so the
+// early launch never takes slots a running grid still needs.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Grid size for a grid-stride kernel: enough CTAs to fill every SM at the
 // kernel's occupancy, never more than `work_ctas`.  Cached per device.
 int persistent_grid(const void* kernel, int threads_per_cta, int64_t work_ctas,

@@ -31,6 +31,7 @@ template <bool LOAD32>
 __global__ void __launch_bounds__(32 * kGainWarps, 3)
 mx_cast_gain_kernel(const uint16_t* __restrict__ w, int64_t N, int K, const float* __restrict__ gamma, float c,
                     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int tiled) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int col = blockIdx.y * kStrip + lane * kGainVec;
   const bool valid = col < K;  // K % 32 == 0: the two lanes of a block agree
@@ -115,16 +116,9 @@ cudaError_t launch_mx_cast_gain(const GainCastArgs& a, cudaStream_t s) {
   if (gx > row_groups) gx = row_groups;
   const dim3 grid((unsigned)gx, (unsigned)strips);
   const int K = (int)a.K;
-  if (load32) {
-    mx_cast_gain_kernel<true><<<grid, 32 * kGainWarps, 0, s>>>(static_cast<const uint16_t*>(a.w), a.N, K, a.gamma,
-                                                               a.c, static_cast<uint8_t*>(a.codes), a.scales,
-                                                               a.scale_tiled);
-  } else {
-    mx_cast_gain_kernel<false><<<grid, 32 * kGainWarps, 0, s>>>(static_cast<const uint16_t*>(a.w), a.N, K, a.gamma,
-                                                                a.c, static_cast<uint8_t*>(a.codes), a.scales,
-                                                                a.scale_tiled);
-  }
-  return cudaGetLastError();
+  return launch_pdl(load32 ? mx_cast_gain_kernel<true> : mx_cast_gain_kernel<false>, grid, dim3(32 * kGainWarps), 0,
+                    s, static_cast<const uint16_t*>(a.w), a.N, K, a.gamma, a.c, static_cast<uint8_t*>(a.codes),
+                    a.scales, a.scale_tiled);
 }
 
 }  // namespace mxnorm

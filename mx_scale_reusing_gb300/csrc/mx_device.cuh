@@ -43,6 +43,19 @@ struct FmtTraits {
                              : (FMT == kFmtE2M1H32 || FMT == kFmtE4M3H32) ? 32 : 0;
 };
 
+// ------------------------------------------------------ dependent launch
+// Programmatic dependent launch (the streaming kernels are launched with
+// programmatic stream serialisation, launch_pdl in launch.h): first let
+// the next grid on the stream be scheduled as this one's CTAs finish, then
+// wait until the previous grid on the stream has completed and its writes
+// are visible.  Called before any global memory access, so stream order is
+// kept; what overlaps is one launch's start with the previous one's end.
+// Without a programmatic predecessor the wait returns at once.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ loads
 // Streaming 16-byte load: read once, keep it out of L1.
 __device__ __forceinline__ uint4 ldg_stream16(const void* p) {

@@ -5,7 +5,9 @@
 //
 // Work split: each warp owns whole rows (grid-stride over T) and walks them
 // as one stream of chunks of 32 * VEC elements (row loop: mx_rows_stream in
-// mx_row.cuh).  Lane l of chunk c holds elements [c*32*VEC + l*VEC, +VEC):
+// mx_row.cuh).  Launched with programmatic stream serialisation (pdl_enter
+// at the top of each kernel), so back-to-back launches overlap one launch's
+// start with the previous one's end.  Lane l of chunk c holds elements [c*32*VEC + l*VEC, +VEC):
 // one 16-, 32- or 64-byte coalesced load.
 //
 // Method: "MXNorm: Reusing MXFP block scales for efficient tensor
@@ -32,6 +34,7 @@ template <int FMT, int VEC, int NCHUNK, int AHEAD, bool EXACT, bool LOAD32, bool
 __global__ void __launch_bounds__(kWarpsPerCta * 32, MINB)
     mx_warp_row_kernel(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
                        uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p, int /*scale_tiled*/) {
+  pdl_enter();
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
   mx_rows_stream<FMT, VEC, NCHUNK, AHEAD, EXACT, LOAD32, ESTIMATE>(x, T, H, codes, scales, inv_rms, p,
@@ -43,6 +46,7 @@ template <int FMT, int VEC, int NCHUNK, int AHEAD, bool ESTIMATE, int MINB, int 
 __global__ void __launch_bounds__(kWarpsPerCta * 32, MINB)
     mx_warp_2row_kernel(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
                         uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p, int /*scale_tiled*/) {
+  pdl_enter();
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
   mx_rows_stream_half<FMT, VEC, NCHUNK, AHEAD, true, ESTIMATE>(x, T, H, codes, scales, inv_rms, p, warp0, nwarps,
@@ -56,7 +60,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
                                uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                float* __restrict__ inv_rms, int p, int scale_tiled) {
   using Tr = FmtTraits<FMT>;
-  const int K = H / kBlock;
+  pdl_enter();
   const int64_t code_row = Tr::fp4 ? (int64_t)(H / 2) : (int64_t)H;
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
@@ -72,10 +76,8 @@ cudaError_t launch_kernel(Kern kern, const WarpRowArgs& a, cudaStream_t stream, 
   const int64_t rows_per_cta = (int64_t)kWarpsPerCta * rows_per_warp;
   const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kWarpsPerCta * 32,
                                    (a.T + rows_per_cta - 1) / rows_per_cta);
-  kern<<<grid, kWarpsPerCta * 32, 0, stream>>>(static_cast<const uint16_t*>(a.x), a.T, (int)a.H,
-                                               static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms, a.p,
-                                               a.scale_tiled);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kWarpsPerCta * 32), 0, stream, static_cast<const uint16_t*>(a.x),
+                    a.T, (int)a.H, static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms, a.p, a.scale_tiled);
 }
 
 // Ring depth (chunks in flight per warp) and occupancy floor (CTAs of 8

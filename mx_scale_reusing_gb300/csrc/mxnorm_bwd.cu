@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
                           const float* __restrict__ inv_rms, int64_t T, int H, uint16_t* __restrict__ dx) {
   constexpr int CE = 32 * VEC;
   const int lane = threadIdx.x & 31;
+  pdl_enter();
   const int nchunk = NCHUNK > 0 ? NCHUNK : (H + CE - 1) / CE;
   constexpr int B = NCHUNK > 0 ? BATCH : 1;
   const int64_t w0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -143,9 +144,8 @@ template <int VEC, int NCHUNK, bool LOAD32>
 cudaError_t launch_one(const BwdArgs& a, cudaStream_t s) {
   auto kern = mxnorm_bwd_ste_kernel<VEC, NCHUNK, 4, 2, LOAD32>;
   const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kWarps * 32, (a.T + kWarps - 1) / kWarps);
-  kern<<<grid, kWarps * 32, 0, s>>>(static_cast<const uint16_t*>(a.x), static_cast<const uint16_t*>(a.dy),
-                                    a.inv_rms, a.T, (int)a.H, static_cast<uint16_t*>(a.dx));
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kWarps * 32), 0, s, static_cast<const uint16_t*>(a.x),
+                    static_cast<const uint16_t*>(a.dy), a.inv_rms, a.T, (int)a.H, static_cast<uint16_t*>(a.dx));
 }
 
 template <bool LOAD32>

@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   static_assert(NCHUNK == 0 || NCHUNK % AHEAD == 0, "the ring must tile the row");
   constexpr int CE = 512;
   const int lane = threadIdx.x & 31;
+  pdl_enter();
   float g = g_arg;
   if (g_dev != nullptr) {
     g = *g_dev;
@@ -175,9 +176,8 @@ cudaError_t launch_one(const Nvfp4Args& a, cudaStream_t s) {
   auto kern = exact ? nvfp4_row_kernel<NCHUNK, AHEAD, true, LOAD32, MINB>
                     : nvfp4_row_kernel<NCHUNK, AHEAD, false, LOAD32, MINB>;
   const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kWarps * 32, (a.T + kWarps - 1) / kWarps);
-  kern<<<grid, kWarps * 32, 0, s>>>(static_cast<const uint16_t*>(a.x), a.T, (int)a.H, a.p, a.g, a.g_dev,
-                                    static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kWarps * 32), 0, s, static_cast<const uint16_t*>(a.x), a.T,
+                    (int)a.H, a.p, a.g, a.g_dev, static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms);
 }
 
 // Four chunks in flight at 2 CTAs/SM time best on GB300 at H = 4096

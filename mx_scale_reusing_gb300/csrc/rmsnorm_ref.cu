@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                         uint16_t* __restrict__ y, float* __restrict__ inv_rms) {
   constexpr int CE = 32 * VEC;
   const int lane = threadIdx.x & 31;
+  pdl_enter();
   const int64_t w0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int64_t nw = (int64_t)gridDim.x * kWarps;
   for (int64_t row = w0; row < T; row += nw) {
@@ -129,9 +130,8 @@ cudaError_t launch_one(const RmsNormArgs& a, cudaStream_t s) {
   auto kern = rmsnorm_bf16_kernel<VEC, NCHUNK>;
   const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kWarps * 32,
                                    (a.T + kWarps - 1) / kWarps);
-  kern<<<grid, kWarps * 32, 0, s>>>(static_cast<const uint16_t*>(a.x), a.T, (int)a.H, a.eps,
-                                    static_cast<uint16_t*>(a.y), a.inv_rms);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kWarps * 32), 0, s, static_cast<const uint16_t*>(a.x), a.T,
+                    (int)a.H, a.eps, static_cast<uint16_t*>(a.y), a.inv_rms);
 }
 
 }  // namespace
