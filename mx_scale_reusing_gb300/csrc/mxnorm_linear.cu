@@ -22,10 +22,13 @@
 // halves, so every w byte crosses L2 -> SM once per pair rather than once per
 // CTA.  Persistent pairs, warp-specialised (11 warps, 352 threads per CTA):
 //   warp 0 lane 0  TMA producer (both CTAs): 2-D tiled loads of the CTA's x
-//                  rows and w half (128-byte swizzle) and of the 512-byte
-//                  scale atoms (its own x atom, both w atoms), all completing
-//                  on the leader's stage "full" mbarrier (cta_group::2 form),
-//                  which expects both CTAs' bytes;
+//                  rows and w half (128-byte swizzle) per stage and, every
+//                  g stages, of the 512-byte scale atoms of those g stages
+//                  (its own x atoms, the atoms of both w halves; one copy
+//                  per operand, since consecutive stages' atoms are
+//                  contiguous), all completing on the leader's stage "full"
+//                  mbarrier (cta_group::2 form), which expects both CTAs'
+//                  bytes;
 //   warp 1 lane 0  leader CTA: MMA issuer.  Per stage it waits for
 //                  "sf_full", issues four tcgen05.mma and commits to the
 //                  "empty" mbarriers of both CTAs (multicast); after a tile's
@@ -70,13 +73,28 @@ constexpr int BM = 128, BN = 256, BK = 128;     // BM rows per CTA (256 per pair
 constexpr int kStages = 6;
 constexpr int kStageA = BM * BK;                 // 16 KiB
 constexpr int kStageB = (BN / 2) * BK;           // 16 KiB: this CTA's half of the tile's w rows
-constexpr int kStageSF = 512 + 2 * 512;          // one A scale atom, both B scale atoms
+// Scale atoms (512 bytes: 128 rows x 4 blocks) of consecutive K stages are
+// contiguous in the MMA layout, so the producer loads those of a group of
+// g = 4, 2 or 1 stages (whichever divides the tile's K stages) with one
+// copy per operand, into a ring of group buffers: the x atoms, then the
+// atoms of both w halves.  The producer refills a buffer only after the
+// stage kStages before the refilling one has completed (its MMAs, so also
+// the scale copies before them), so the last stage of the group the buffer
+// held must lie at least kStages back: (groups - 1) g + 1 >= kStages, a
+// ring of ceil((kStages - 1) / g) + 1 groups: 3, 4 or 6.
+constexpr int kSfRing = 3 * 4 * 3 * 512;          // 18 KiB: the largest ring (3 groups of 4 stages)
 constexpr int kEpiWarps = 8;                     // two per TMEM lane quadrant, 128 columns each
 constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTxBytes = kStageA + kStageB + kStageSF;  // one CTA's bytes per stage
+constexpr uint32_t kTxBytes = kStageA + kStageB;  // one CTA's operand bytes per stage
 constexpr unsigned long long kWaitNs = 2000000000ull;
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * (kStageA + kStageB + kStageSF) + 256;
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * (kStageA + kStageB) + kSfRing + 256;
+
+__host__ __device__ constexpr int sf_ring_groups(int g) { return (kStages - 1 + g - 1) / g + 1; }
+static_assert(sf_ring_groups(4) * 3 * 4 * 512 <= kSfRing && sf_ring_groups(2) * 3 * 2 * 512 <= kSfRing &&
+                  sf_ring_groups(1) * 3 * 512 <= kSfRing,
+              "every scale-group ring fits its shared memory");
+
 
 __device__ __forceinline__ uint32_t saddr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -230,13 +248,14 @@ template <bool kV8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mxfp8_linear_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                         const __grid_constant__ CUtensorMap tm_sfx, const __grid_constant__ CUtensorMap tm_sfw,
-                        const float* __restrict__ inv_rms, uint16_t* __restrict__ out, int64_t T, int K, int N) {
+                        const float* __restrict__ inv_rms, uint16_t* __restrict__ out, int64_t T, int K, int N,
+                        int sf_group) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kStageA;
   uint8_t* sSF = sB + kStages * kStageB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sSF + kStages * kStageSF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSF + kSfRing);
   // bars: full[kStages], empty[kStages], sf_full[kStages], acc_full, acc_empty, drain, drain_sf;
   // then the TMEM base word.  The leader's full[s] counts both CTAs' bytes; the peer uses only
   // empty[] and acc_full.
@@ -250,6 +269,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
   const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int num_n = N / BN, num_kt = K / BK;
+  const int sf_bufs = sf_ring_groups(sf_group), sf_bytes = 3 * sf_group * 512;
   const int64_t num_m = (T + 2 * BM - 1) / (2 * BM);  // 256-row tiles
   const int64_t row_atoms = (T + BM - 1) / BM;          // 128-row scale atoms of x
   const int64_t tiles = num_m * num_n;
@@ -280,6 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       int64_t it = 0;
+      int sf_pos = 0, sf_buf = 0;  // stage within its scale group, the group's ring buffer
       bool ok = true;
       for (int64_t tile = pair; tile < tiles && ok; tile += npairs) {
         int64_t mt;
@@ -293,16 +314,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t use = (uint32_t)(it / kStages);
           if (use > 0 && !(ok = wait_bounded(empty0 + 8 * s, (use - 1) & 1u))) break;
           const uint32_t fb = map_to_rank(full0 + 8 * s, 0);  // the leader's stage barrier
+          const bool group_start = sf_pos == 0;  // groups tile the K stages of every tile
           if (rank == 0)
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full0 + 8 * s), "r"(2 * kTxBytes)
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full0 + 8 * s),
+                         "r"(2 * (kTxBytes + (group_start ? (uint32_t)sf_bytes : 0u)))
                          : "memory");
           tma_2d_pair(saddr(sA + s * kStageA), &tm_x, kt * BK, (int)xrow, fb);
           tma_2d_pair(saddr(sB + s * kStageB), &tm_w, kt * BK, nt * BN + (int)rank * (BN / 2), fb);
-          // scale atoms: 512 bytes = 4 rows of the 128-byte-wide scale maps
-          const uint32_t sf = saddr(sSF + s * kStageSF);
-          tma_2d_pair(sf, &tm_sfx, 0, (int)(4 * (xatom * num_kt + kt)), fb);
-          tma_2d_pair(sf + 512, &tm_sfw, 0, (int)(4 * ((int64_t)(2 * nt) * num_kt + kt)), fb);
-          tma_2d_pair(sf + 1024, &tm_sfw, 0, (int)(4 * ((int64_t)(2 * nt + 1) * num_kt + kt)), fb);
+          if (group_start) {
+            // the group's scale atoms: 4 rows of the 128-byte-wide scale maps each
+            const uint32_t sf = saddr(sSF + sf_buf * sf_bytes);
+            tma_2d_pair(sf, &tm_sfx, 0, (int)(4 * (xatom * num_kt + kt)), fb);
+            tma_2d_pair(sf + sf_group * 512, &tm_sfw, 0, (int)(4 * ((int64_t)(2 * nt) * num_kt + kt)), fb);
+            tma_2d_pair(sf + 2 * sf_group * 512, &tm_sfw, 0, (int)(4 * ((int64_t)(2 * nt + 1) * num_kt + kt)), fb);
+          }
+          if (++sf_pos == sf_group) {
+            sf_pos = 0;
+            if (++sf_buf == sf_bufs) sf_buf = 0;
+          }
         }
       }
       // every copy issued (both CTAs') must have landed before the pair may
@@ -365,15 +394,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // only after the MMAs that read the slot completed.
       const int64_t my_tiles = pair < tiles ? (tiles - 1 - pair) / npairs + 1 : 0;
       const int64_t total = my_tiles * num_kt;
+      int sf_pos = 0, sf_buf = 0;  // the producer's scale-group walk, in step with it
       for (int64_t it = 0; it < total; ++it) {
         const int s = (int)(it % kStages);
         if (!wait_bounded(full0 + 8 * s, (uint32_t)(it / kStages) & 1u)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t tsf = tmem + 256 + 16 * s;
-        const uint32_t sf = saddr(sSF + s * kStageSF);
+        const uint32_t sf = saddr(sSF + sf_buf * sf_bytes) + (uint32_t)(sf_pos * 512);
+        if (++sf_pos == sf_group) {
+          sf_pos = 0;
+          if (++sf_buf == sf_bufs) sf_buf = 0;
+        }
         asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf), "l"(desc_atom(sf)));
-        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 4), "l"(desc_atom(sf + 512)));
-        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 8), "l"(desc_atom(sf + 1024)));
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 4),
+                     "l"(desc_atom(sf + sf_group * 512)));
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 8),
+                     "l"(desc_atom(sf + 2 * sf_group * 512)));
         asm volatile(
             "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
                 sf_full0 + 8 * s),
@@ -493,13 +529,13 @@ cudaError_t resident_pairs(const void* kern, int variant, int* out) {
 }
 
 // MMA-layout scale bytes viewed as rows of 128 bytes (a 512-byte atom is 4
-// rows), box of 4 rows, no swizzle: one TMA load per atom.
-bool encode_scales(CUtensorMap* map, const void* base, int64_t bytes) {
+// rows), box of 4 g rows, no swizzle: one TMA load per group of g atoms.
+bool encode_scales(CUtensorMap* map, const void* base, int64_t bytes, int g) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {128, (cuuint64_t)(bytes / 128)};
   cuuint64_t strides[1] = {128};
-  cuuint32_t box[2] = {128, 4};
+  cuuint32_t box[2] = {128, (cuuint32_t)(4 * g)};
   cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -510,11 +546,13 @@ bool encode_scales(CUtensorMap* map, const void* base, int64_t bytes) {
 
 cudaError_t launch_mxfp8_linear(const LinearArgs& a, cudaStream_t s) {
   CUtensorMap tm_x, tm_w, tm_sfx, tm_sfw;
-  const int64_t sfx_bytes = ((a.T + BM - 1) / BM) * (a.K / BK) * 512;
-  const int64_t sfw_bytes = ((a.N + BM - 1) / BM) * (a.K / BK) * 512;
+  const int64_t num_kt = a.K / BK;
+  const int g = num_kt % 4 == 0 ? 4 : num_kt % 2 == 0 ? 2 : 1;  // scale atoms loaded per copy
+  const int64_t sfx_bytes = ((a.T + BM - 1) / BM) * num_kt * 512;
+  const int64_t sfw_bytes = ((a.N + BM - 1) / BM) * num_kt * 512;
   if (!encode_codes(&tm_x, a.x_codes, a.T, a.K, BM) || !encode_codes(&tm_w, a.w_codes, a.N, a.K, BN / 2) ||
-      !encode_scales(&tm_sfx, a.x_scales, sfx_bytes) ||
-      !encode_scales(&tm_sfw, a.w_scales, sfw_bytes))
+      !encode_scales(&tm_sfx, a.x_scales, sfx_bytes, g) ||
+      !encode_scales(&tm_sfw, a.w_scales, sfw_bytes, g))
     return cudaErrorInvalidValue;
   // rows start 32-byte aligned when out is (N is a multiple of 256)
   const bool v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
@@ -533,11 +571,11 @@ cudaError_t launch_mxfp8_linear(const LinearArgs& a, cudaStream_t s) {
   if (v8)
     mxfp8_linear_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, tm_sfx, tm_sfw, a.inv_rms,
                                                                  static_cast<uint16_t*>(a.out), a.T, (int)a.K,
-                                                                 (int)a.N);
+                                                                 (int)a.N, g);
   else
     mxfp8_linear_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, tm_sfx, tm_sfw, a.inv_rms,
                                                                   static_cast<uint16_t*>(a.out), a.T, (int)a.K,
-                                                                  (int)a.N);
+                                                                  (int)a.N, g);
   return cudaGetLastError();
 }
 

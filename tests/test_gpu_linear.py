@@ -117,9 +117,22 @@ def linear_case(T, K, N, seed, rows=None, out_offset=0):
     return got, want
 
 
-@pytest.mark.parametrize("T,K,N", [(128, 128, 256), (200, 256, 512), (1000, 768, 768), (131, 4096, 256)])
+@pytest.mark.parametrize("T,K,N", [(128, 128, 256), (200, 256, 512), (1000, 768, 768), (131, 4096, 256),
+                                   (77, 384, 256), (260, 1152, 512), (129, 640, 256)])
 def test_linear_small(T, K, N):
+    """K stage counts of 1 to 32, odd and even: the producer loads the scale
+    atoms of 1, 2 or 4 stages per copy, whichever divides the count."""
     linear_case(T, K, N, seed=T + K + N)
+
+
+@pytest.mark.parametrize("K", [768, 1152])
+def test_linear_many_tiles_scale_groups_of_2_and_1(K):
+    """Many tiles per CTA pair with scale atoms loaded 2 (K = 768) or 1
+    (K = 1152) stages per copy, so the scale-group ring wraps across tile
+    boundaries many times; sampled rows of every row tile."""
+    T = 8192 + 77
+    rows = np.unique(np.concatenate([np.arange(0, T, 257), np.arange(T - 4, T)]))
+    linear_case(T, K, 2048, seed=K, rows=rows)
 
 
 def test_linear_llama3_8b_layer_sampled():
