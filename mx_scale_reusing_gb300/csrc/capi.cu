@@ -57,6 +57,15 @@ int check_common(const void* x, int64_t T, int64_t H, const void* codes, const v
 
 void set_last_error(const char* msg) { g_last_error = msg; }
 
+bool is_device_memory(const void* p) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    (void)cudaGetLastError();  // leave no sticky error behind for the launch check
+    return false;
+  }
+  return attr.type == cudaMemoryTypeDevice;
+}
+
 int persistent_grid(const void* kernel, int threads, int64_t work_ctas, size_t dyn_smem) {
   int dev = 0;
   cudaGetDevice(&dev);

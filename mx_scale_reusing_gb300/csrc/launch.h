@@ -19,6 +19,10 @@ struct WarpRowArgs {
   int scale_tiled = 0;  // 1: scales in the MMA atom layout (see scale_ptr in mx_row.cuh)
 };
 
+// True when p points into device memory (not mapped host or managed memory):
+// the streaming kernels prefetch their first rows into L2 only then.
+bool is_device_memory(const void* p);
+
 struct RmsNormArgs {
   const void* x;      // bf16 [T, H]
   int64_t T;

@@ -51,9 +51,24 @@ struct FmtTraits {
 // are visible.  Called before any global memory access, so stream order is
 // kept; what overlaps is one launch's start with the previous one's end.
 // Without a programmatic predecessor the wait returns at once.
-__device__ __forceinline__ void pdl_enter() {
+__device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+  pdl_launch_dependents();
+  pdl_wait();
+}
+
+// Bring `bytes` (a multiple of 16, p 16-byte aligned) at p into L2 without
+// waiting (the TMA engine's bulk prefetch).  A hint with no effect on memory
+// semantics: L2 is the GPU's point of coherence, so a line prefetched
+// before a predecessor kernel writes it is updated in place.  The streaming
+// kernels issue it for their first rows between pdl_launch_dependents and
+// pdl_wait, so the first DRAM round trip overlaps the previous kernel's end.
+// Device memory only (the launcher checks): never at mapped host memory.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // ------------------------------------------------------------------ loads

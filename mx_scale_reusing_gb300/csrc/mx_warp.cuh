@@ -5,9 +5,11 @@
 //
 // Work split: each warp owns whole rows (grid-stride over T) and walks them
 // as one stream of chunks of 32 * VEC elements (row loop: mx_rows_stream in
-// mx_row.cuh).  Launched with programmatic stream serialisation (pdl_enter
-// at the top of each kernel), so back-to-back launches overlap one launch's
-// start with the previous one's end.  Lane l of chunk c holds elements [c*32*VEC + l*VEC, +VEC):
+// mx_row.cuh).  Launched with programmatic stream serialisation, so
+// back-to-back launches overlap one launch's start with the previous one's
+// end: each kernel first lets the next grid be scheduled, prefetches its
+// warps' first rows into L2 (device memory only), then waits for the
+// previous grid before any load.  Lane l of chunk c holds elements [c*32*VEC + l*VEC, +VEC):
 // one 16-, 32- or 64-byte coalesced load.
 //
 // Method: "MXNorm: Reusing MXFP block scales for efficient tensor
@@ -33,10 +35,13 @@ constexpr int kWarpsPerCta = 8;
 template <int FMT, int VEC, int NCHUNK, int AHEAD, bool EXACT, bool LOAD32, bool ESTIMATE, int MINB, int TILED>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, MINB)
     mx_warp_row_kernel(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
-                       uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p, int /*scale_tiled*/) {
-  pdl_enter();
+                       uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p, int /*scale_tiled*/,
+                       int l2_prefetch) {
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+  pdl_launch_dependents();
+  if (l2_prefetch && (threadIdx.x & 31) == 0 && warp0 < T) prefetch_l2(x + warp0 * (int64_t)H, (uint32_t)(2 * H));
+  pdl_wait();
   mx_rows_stream<FMT, VEC, NCHUNK, AHEAD, EXACT, LOAD32, ESTIMATE>(x, T, H, codes, scales, inv_rms, p,
                                                                    warp0, nwarps, TILED);
 }
@@ -45,10 +50,14 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, MINB)
 template <int FMT, int VEC, int NCHUNK, int AHEAD, bool ESTIMATE, int MINB, int TILED>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, MINB)
     mx_warp_2row_kernel(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
-                        uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p, int /*scale_tiled*/) {
-  pdl_enter();
+                        uint8_t* __restrict__ scales, float* __restrict__ inv_rms, int p, int /*scale_tiled*/,
+                        int l2_prefetch) {
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+  pdl_launch_dependents();
+  if (l2_prefetch && (threadIdx.x & 31) == 0 && 2 * warp0 < T)  // the warp's first pair of rows
+    prefetch_l2(x + 2 * warp0 * (int64_t)H, (uint32_t)(2 * H * (2 * warp0 + 1 < T ? 2 : 1)));
+  pdl_wait();
   mx_rows_stream_half<FMT, VEC, NCHUNK, AHEAD, true, ESTIMATE>(x, T, H, codes, scales, inv_rms, p, warp0, nwarps,
                                                                TILED);
 }
@@ -58,9 +67,13 @@ template <int FMT, int VEC, bool LOAD32, bool ESTIMATE>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     mx_warp_row_generic_kernel(const uint16_t* __restrict__ x, int64_t T, int H,
                                uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                               float* __restrict__ inv_rms, int p, int scale_tiled) {
+                               float* __restrict__ inv_rms, int p, int scale_tiled, int l2_prefetch) {
   using Tr = FmtTraits<FMT>;
-  pdl_enter();
+  const int64_t w0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  pdl_launch_dependents();
+  if (l2_prefetch && (threadIdx.x & 31) == 0 && w0 < T)  // up to 64 KiB of the warp's first row
+    prefetch_l2(x + w0 * (int64_t)H, (uint32_t)min(2 * H, 65536));
+  pdl_wait();
   const int64_t code_row = Tr::fp4 ? (int64_t)(H / 2) : (int64_t)H;
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
@@ -77,7 +90,8 @@ cudaError_t launch_kernel(Kern kern, const WarpRowArgs& a, cudaStream_t stream, 
   const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kWarpsPerCta * 32,
                                    (a.T + rows_per_cta - 1) / rows_per_cta);
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kWarpsPerCta * 32), 0, stream, static_cast<const uint16_t*>(a.x),
-                    a.T, (int)a.H, static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms, a.p, a.scale_tiled);
+                    a.T, (int)a.H, static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms, a.p, a.scale_tiled,
+                    is_device_memory(a.x) ? 1 : 0);
 }
 
 // Ring depth (chunks in flight per warp) and occupancy floor (CTAs of 8
