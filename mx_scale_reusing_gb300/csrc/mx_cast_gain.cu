@@ -30,9 +30,18 @@ constexpr int kRowsAhead = 4;             // rows whose loads are issued togethe
 template <bool LOAD32>
 __global__ void __launch_bounds__(32 * kGainWarps, 3)
 mx_cast_gain_kernel(const uint16_t* __restrict__ w, int64_t N, int K, const float* __restrict__ gamma, float c,
-                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int tiled) {
-  pdl_enter();
+                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int tiled, int l2_prefetch) {
   const int lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  {
+    // lanes 0..kRowsAhead-1 prefetch the warp's strip of its first rows into
+    // L2 while the previous launch ends (device memory only)
+    const int64_t r = (int64_t)blockIdx.x * kGainWarps + (threadIdx.x >> 5) + (int64_t)lane * gridDim.x * kGainWarps;
+    const int c0 = blockIdx.y * kStrip;
+    if (l2_prefetch && lane < kRowsAhead && r < N)
+      prefetch_l2(w + r * (int64_t)K + c0, (uint32_t)(2 * min(kStrip, K - c0)));
+  }
+  pdl_wait();
   const int col = blockIdx.y * kStrip + lane * kGainVec;
   const bool valid = col < K;  // K % 32 == 0: the two lanes of a block agree
   const int KB = K / kBlock;
@@ -118,7 +127,7 @@ cudaError_t launch_mx_cast_gain(const GainCastArgs& a, cudaStream_t s) {
   const int K = (int)a.K;
   return launch_pdl(load32 ? mx_cast_gain_kernel<true> : mx_cast_gain_kernel<false>, grid, dim3(32 * kGainWarps), 0,
                     s, static_cast<const uint16_t*>(a.w), a.N, K, a.gamma, a.c, static_cast<uint8_t*>(a.codes),
-                    a.scales, a.scale_tiled);
+                    a.scales, a.scale_tiled, is_device_memory(a.w) ? 1 : 0);
 }
 
 }  // namespace mxnorm
