@@ -54,6 +54,15 @@
  * the legacy default stream) and the call returns.  Outputs are fully
  * written when the stream reaches the kernel's end; after an error return
  * they are unspecified.  Inputs and outputs must not overlap.
+ * The streaming kernels (the fused pass, NVFP4, the backward, the RMSNorm
+ * baseline's first kernel, the gain-folded cast) are launched with
+ * programmatic stream serialisation: each may be scheduled while the
+ * previous kernel on the stream finishes, waits for that kernel's
+ * completion before touching memory, and lets the next kernel be
+ * scheduled early.  Stream order holds as usual; a kernel of the caller's
+ * launched after one of them with the programmatic-serialisation attribute
+ * must, as any programmatic dependent, wait (griddepcontrol.wait,
+ * cudaGridDependencySynchronize) before reading its outputs.
  *
  * Errors.  Arguments are checked on the host before any launch:
  *   T < 0, H <= 0, H % 32 != 0, p not in {1, 2}, unknown fmt or variant,

@@ -83,10 +83,17 @@ __device__ __forceinline__ void store_dx(uint16_t* dst, const uint32_t (&wx)[VEC
 template <int VEC, int NCHUNK, int BATCH, int MINB, bool LOAD32>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
     mxnorm_bwd_ste_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ dy,
-                          const float* __restrict__ inv_rms, int64_t T, int H, uint16_t* __restrict__ dx) {
+                          const float* __restrict__ inv_rms, int64_t T, int H, uint16_t* __restrict__ dx,
+                          int l2_prefetch) {
   constexpr int CE = 32 * VEC;
   const int lane = threadIdx.x & 31;
-  pdl_enter();
+  pdl_launch_dependents();
+  {
+    const int64_t r0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);  // the warp's first row of x and dy
+    if (l2_prefetch && lane < 2 && r0 < T)
+      prefetch_l2((lane == 0 ? x : dy) + r0 * (int64_t)H, (uint32_t)min(2 * H, 65536));
+  }
+  pdl_wait();
   const int nchunk = NCHUNK > 0 ? NCHUNK : (H + CE - 1) / CE;
   constexpr int B = NCHUNK > 0 ? BATCH : 1;
   const int64_t w0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -145,7 +152,8 @@ cudaError_t launch_one(const BwdArgs& a, cudaStream_t s) {
   auto kern = mxnorm_bwd_ste_kernel<VEC, NCHUNK, 4, 2, LOAD32>;
   const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kWarps * 32, (a.T + kWarps - 1) / kWarps);
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kWarps * 32), 0, s, static_cast<const uint16_t*>(a.x),
-                    static_cast<const uint16_t*>(a.dy), a.inv_rms, a.T, (int)a.H, static_cast<uint16_t*>(a.dx));
+                    static_cast<const uint16_t*>(a.dy), a.inv_rms, a.T, (int)a.H, static_cast<uint16_t*>(a.dx),
+                    is_device_memory(a.x) && is_device_memory(a.dy) ? 1 : 0);
 }
 
 template <bool LOAD32>

@@ -90,11 +90,16 @@ template <int NCHUNK, int AHEAD, bool EXACT, bool LOAD32, int MINB>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
     nvfp4_row_kernel(const uint16_t* __restrict__ x, int64_t T, int H, int p, float g_arg,
                      const float* __restrict__ g_dev, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                     float* __restrict__ inv_rms) {
+                     float* __restrict__ inv_rms, int l2_prefetch) {
   static_assert(NCHUNK == 0 || NCHUNK % AHEAD == 0, "the ring must tile the row");
   constexpr int CE = 512;
   const int lane = threadIdx.x & 31;
-  pdl_enter();
+  pdl_launch_dependents();
+  {
+    const int64_t r0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);  // the warp's first row
+    if (l2_prefetch && lane == 0 && r0 < T) prefetch_l2(x + r0 * (int64_t)H, (uint32_t)min(2 * H, 65536));
+  }
+  pdl_wait();
   float g = g_arg;
   if (g_dev != nullptr) {
     g = *g_dev;
@@ -177,7 +182,8 @@ cudaError_t launch_one(const Nvfp4Args& a, cudaStream_t s) {
                     : nvfp4_row_kernel<NCHUNK, AHEAD, false, LOAD32, MINB>;
   const int grid = persistent_grid(reinterpret_cast<const void*>(kern), kWarps * 32, (a.T + kWarps - 1) / kWarps);
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kWarps * 32), 0, s, static_cast<const uint16_t*>(a.x), a.T,
-                    (int)a.H, a.p, a.g, a.g_dev, static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms);
+                    (int)a.H, a.p, a.g, a.g_dev, static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms,
+                    is_device_memory(a.x) ? 1 : 0);
 }
 
 // Four chunks in flight at 2 CTAs/SM time best on GB300 at H = 4096
