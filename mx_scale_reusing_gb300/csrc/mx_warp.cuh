@@ -8,8 +8,9 @@
 // mx_row.cuh).  Launched with programmatic stream serialisation, so
 // back-to-back launches overlap one launch's start with the previous one's
 // end: each kernel first lets the next grid be scheduled, prefetches its
-// warps' first rows into L2 (device memory only), then waits for the
-// previous grid before any load.  Lane l of chunk c holds elements [c*32*VEC + l*VEC, +VEC):
+// warps' first rows into L2 (device memory only; all of them when the whole
+// input fits in a quarter of L2), then waits for the previous grid before
+// any load.  Lane l of chunk c holds elements [c*32*VEC + l*VEC, +VEC):
 // one 16-, 32- or 64-byte coalesced load.
 //
 // Method: "MXNorm: Reusing MXFP block scales for efficient tensor
@@ -28,6 +29,20 @@ namespace warp_row {
 
 constexpr int kWarpsPerCta = 8;
 
+// L2 prefetch before the dependent-launch wait: 0 none (x in host memory),
+// 1 each warp's first row (or pair of rows), 2 up to 32 of each warp's rows,
+// taken when the whole input fits in kWholeInputPrefetchBytes (a quarter of
+// L2).  Mode 2 measured 5 % faster at 16384 x 768 (25 MB in) and 3 % slower
+// at 32768 x 2048 (128 MiB in), where it would cover a quarter of the rows.
+constexpr int64_t kWholeInputPrefetchBytes = (int64_t)32 << 20;
+
+__device__ __forceinline__ int prefetch_lanes(int mode) { return mode == 2 ? 32 : mode; }
+
+inline int prefetch_mode(const WarpRowArgs& a) {
+  if (!is_device_memory(a.x)) return 0;
+  return a.T * a.H * 2 <= kWholeInputPrefetchBytes ? 2 : 1;
+}
+
 // MINB: CTAs per SM the register allocation must allow (occupancy floor).
 // TILED: the scale layout (0 row-major, 1 MMA atoms) as a compile-time
 // constant; taken at run time it cost up to a fifth of the bandwidth on
@@ -40,7 +55,11 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, MINB)
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
   pdl_launch_dependents();
-  if (l2_prefetch && (threadIdx.x & 31) == 0 && warp0 < T) prefetch_l2(x + warp0 * (int64_t)H, (uint32_t)(2 * H));
+  {
+    // lane l prefetches the warp's l-th row: lane 0 alone in mode 1, up to 32 rows in mode 2
+    const int64_t r = warp0 + (int64_t)(threadIdx.x & 31) * nwarps;
+    if ((threadIdx.x & 31) < prefetch_lanes(l2_prefetch) && r < T) prefetch_l2(x + r * (int64_t)H, (uint32_t)(2 * H));
+  }
   pdl_wait();
   mx_rows_stream<FMT, VEC, NCHUNK, AHEAD, EXACT, LOAD32, ESTIMATE>(x, T, H, codes, scales, inv_rms, p,
                                                                    warp0, nwarps, TILED);
@@ -55,8 +74,12 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, MINB)
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
   pdl_launch_dependents();
-  if (l2_prefetch && (threadIdx.x & 31) == 0 && 2 * warp0 < T)  // the warp's first pair of rows
-    prefetch_l2(x + 2 * warp0 * (int64_t)H, (uint32_t)(2 * H * (2 * warp0 + 1 < T ? 2 : 1)));
+  {
+    // lane l prefetches the warp's l-th pair of rows (lane 0 alone in mode 1)
+    const int64_t pr = warp0 + (int64_t)(threadIdx.x & 31) * nwarps;
+    if ((threadIdx.x & 31) < prefetch_lanes(l2_prefetch) && 2 * pr < T)
+      prefetch_l2(x + 2 * pr * (int64_t)H, (uint32_t)(2 * H * (2 * pr + 1 < T ? 2 : 1)));
+  }
   pdl_wait();
   mx_rows_stream_half<FMT, VEC, NCHUNK, AHEAD, true, ESTIMATE>(x, T, H, codes, scales, inv_rms, p, warp0, nwarps,
                                                                TILED);
@@ -91,7 +114,7 @@ cudaError_t launch_kernel(Kern kern, const WarpRowArgs& a, cudaStream_t stream, 
                                    (a.T + rows_per_cta - 1) / rows_per_cta);
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kWarpsPerCta * 32), 0, stream, static_cast<const uint16_t*>(a.x),
                     a.T, (int)a.H, static_cast<uint8_t*>(a.codes), a.scales, a.inv_rms, a.p, a.scale_tiled,
-                    is_device_memory(a.x) ? 1 : 0);
+                    prefetch_mode(a));
 }
 
 // Ring depth (chunks in flight per warp) and occupancy floor (CTAs of 8
