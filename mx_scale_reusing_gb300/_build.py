@@ -18,7 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmxnorm.so")
-SOURCES = ["capi.cu", "mxnorm_warp.cu", "mxnorm_warp_fp8.cu", "mxnorm_warp_fp4.cu", "mxnorm_tiled.cu",
+SOURCES = ["capi.cu", "mxnorm_warp.cu", "mxnorm_warp_fp8.cu", "mxnorm_warp_fp8_cast.cu", "mxnorm_warp_fp8_h16.cu",
+           "mxnorm_warp_fp8_h32.cu", "mxnorm_warp_fp4.cu", "mxnorm_warp_fp4_h16.cu", "mxnorm_warp_fp4_h32.cu",
+           "mxnorm_tiled.cu",
            "rmsnorm_ref.cu", "rmsnorm_static_ws.cu", "mxnorm_bwd.cu",
            "mxnorm_nvfp4.cu", "mxnorm_linear.cu", "mx_cast_gain.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,7 +1,7 @@
 // mx_warp.cuh -- the one-row-per-warp MXNorm kernel templates and their
-// launch-shape selection, instantiated per format family by
-// mxnorm_warp_fp8.cu and mxnorm_warp_fp4.cu (split so the two compile in
-// parallel).
+// launch-shape selection, instantiated one format per translation unit
+// (mxnorm_warp_fp8*.cu, mxnorm_warp_fp4*.cu) so the formats compile in
+// parallel.
 //
 // Work split: each warp owns whole rows (grid-stride over T) and walks them
 // as one stream of chunks of 32 * VEC elements (row loop: mx_rows_stream in
@@ -242,8 +242,14 @@ cudaError_t launch_fmt(const WarpRowArgs& a, cudaStream_t s) {
 
 }  // namespace warp_row
 
-// Per-family entry points (mxnorm_warp_fp8.cu / mxnorm_warp_fp4.cu).
-cudaError_t launch_warp_row_fp8(const WarpRowArgs& a, cudaStream_t s, bool estimate);
-cudaError_t launch_warp_row_fp4(const WarpRowArgs& a, cudaStream_t s);
+// Per-format entry points, one translation unit each (mxnorm_warp_fp8*.cu,
+// mxnorm_warp_fp4*.cu); _cast is the E4M3 cast without the estimate.
+cudaError_t launch_warp_row_e4m3(const WarpRowArgs& a, cudaStream_t s);
+cudaError_t launch_warp_row_e4m3_cast(const WarpRowArgs& a, cudaStream_t s);
+cudaError_t launch_warp_row_e4m3_h16(const WarpRowArgs& a, cudaStream_t s);
+cudaError_t launch_warp_row_e4m3_h32(const WarpRowArgs& a, cudaStream_t s);
+cudaError_t launch_warp_row_e2m1(const WarpRowArgs& a, cudaStream_t s);
+cudaError_t launch_warp_row_e2m1_h16(const WarpRowArgs& a, cudaStream_t s);
+cudaError_t launch_warp_row_e2m1_h32(const WarpRowArgs& a, cudaStream_t s);
 
 }  // namespace mxnorm

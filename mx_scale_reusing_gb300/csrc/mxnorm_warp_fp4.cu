@@ -1,17 +1,12 @@
-// mxnorm_warp_fp4.cu -- warp-row kernels for the FP4 E2M1 formats (plain,
-// H16, H32).
+// mxnorm_warp_fp4.cu -- warp-row kernels for the MXNorm pass for FP4 E2M1
+// codes (no rotation).  One format per translation unit, so the formats
+// compile in parallel.
 #include "mx_warp.cuh"
 
 namespace mxnorm {
 
-cudaError_t launch_warp_row_fp4(const WarpRowArgs& a, cudaStream_t s) {
-  using namespace warp_row;
-  switch (a.fmt) {
-    case kFmtE2M1: return launch_fmt<kFmtE2M1, true>(a, s);
-    case kFmtE2M1H16: return launch_fmt<kFmtE2M1H16, true>(a, s);
-    case kFmtE2M1H32: return launch_fmt<kFmtE2M1H32, true>(a, s);
-    default: return cudaErrorInvalidValue;
-  }
+cudaError_t launch_warp_row_e2m1(const WarpRowArgs& a, cudaStream_t s) {
+  return warp_row::launch_fmt<kFmtE2M1, true>(a, s);
 }
 
 }  // namespace mxnorm
