@@ -786,13 +786,22 @@ def run_profile_case(args):
         out = torch.empty((T, Nw), dtype=torch.bfloat16, device="cuda")
         torch.cuda.synchronize()
 
+        a8, b8 = xc.view(torch.float8_e4m3fn), w_codes.view(torch.float8_e4m3fn)
+
         def fn_lin(i):
             mx.linear_fwd(xc, xs, xinv, w_codes, w_scales, out=out, stream=stream)
+            if args.profile_with_cublaslt:
+                with torch.cuda.stream(stream):
+                    torch._scaled_mm(a8, b8.t(), scale_a=xs.view(torch.float8_e8m0fnu),
+                                     scale_b=w_scales.view(torch.float8_e8m0fnu), out_dtype=torch.bfloat16)
         m = time_region(torch, stream, fn_lin, args.steps, args.warmup, 1)
-        print(json.dumps({"profile_only": True, "kernel": "mxnorm_linear_fwd", "T": T, "K": H, "N": Nw,
-                          "mean_launch_ms": round(m, 6),
-                          "TFLOP/s": round(2.0 * T * H * Nw / (m * 1e-3) / 1e12, 1),
-                          "device_errors": mx.device_errors()}), flush=True)
+        rec = {"profile_only": True, "kernel": "mxnorm_linear_fwd", "T": T, "K": H, "N": Nw,
+               "mean_launch_ms": round(m, 6), "TFLOP/s": round(2.0 * T * H * Nw / (m * 1e-3) / 1e12, 1),
+               "device_errors": mx.device_errors()}
+        if args.profile_with_cublaslt:  # a step is both GEMMs
+            rec.update({"kernel": "mxnorm_linear_fwd + cuBLASLt", "mean_step_ms": rec.pop("mean_launch_ms")})
+            del rec["TFLOP/s"]
+        print(json.dumps(rec), flush=True)
         return
     if args.profile_baseline:
         y = torch.empty_like(x)
@@ -874,6 +883,9 @@ def main():
     ap.add_argument("--profile-linear", action="store_true",
                     help="profiling case: MXNormLinear's GEMM (mxnorm_linear_fwd) on the first N rows "
                          "against a 4096 x 4096 weight")
+    ap.add_argument("--profile-with-cublaslt", action="store_true",
+                    help="with --profile-linear: each step also runs cuBLASLt's MXFP8 GEMM on the same "
+                         "codes and scales, so one capture holds both kernels")
     ap.add_argument("--profile-bwd", action="store_true",
                     help="profiling case: the STE backward (mxnorm_bwd_ste) on the first N rows")
     ap.add_argument("--profile-nvfp4", action="store_true",
