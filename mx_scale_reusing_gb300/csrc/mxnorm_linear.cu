@@ -40,11 +40,11 @@
 //                  itself would wait between its stages; from a thread of
 //                  their own they overlap the MMAs in flight;
 //   warps 3-10     epilogue (both CTAs), two per TMEM lane quadrant (32 rows)
-//                  with 128 columns each: tcgen05.ld of the fp32
-//                  accumulators in two 64-column steps, times rho~[row],
-//                  rounded to packed bf16 in registers; after the second
-//                  load an arrival on the leader's "acc_empty" (16 per tile)
-//                  frees TMEM for the next tile's MMAs, and each lane stores
+//                  with 128 columns each: tcgen05.ld of all 128 fp32
+//                  accumulators at once (one wait), then an arrival on the
+//                  leader's "acc_empty" (16 per tile) frees TMEM for the
+//                  next tile's MMAs; the values are multiplied by rho~[row],
+//                  rounded to packed bf16 in registers, and each lane stores
 //                  its row's 128 outputs straight to global memory (32-byte
 //                  stores when out is 32-byte aligned, else 16-byte ones).
 // Each CTA's tensor core reads the B scales of all 256 columns from its own
@@ -441,23 +441,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int c0 = nt * BN + 128 * half;
       const float r = row < T ? inv_rms[row] : 0.0f;
       const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(128 * half);
-      // Read the warp's 32 x 128 share of the accumulators, then hand TMEM
-      // back to the MMA issuer before the second half is converted and the
-      // row is stored: the next tile's MMAs overlap both.
-      uint32_t o[64];
-      {
-        uint32_t v[64];
-        tmem_load64(taddr, v);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        scale_pack64(v, r, o);
-      }
-      uint32_t v[64];
-      tmem_load64(taddr + 64, v);
+      // Read the warp's 32 x 128 share of the accumulators (all four loads
+      // in flight, one wait), then hand TMEM back to the MMA issuer before
+      // the row is converted and stored: the next tile's MMAs overlap both.
+      uint32_t v[128];
+      tmem_load64(taddr, *reinterpret_cast<uint32_t(*)[64]>(v));
+      tmem_load64(taddr + 64, *reinterpret_cast<uint32_t(*)[64]>(v + 64));
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) arrive_remote(acc_empty_leader);
-      scale_pack64(v, r, o + 32);
+      uint32_t o[64];
+      scale_pack64(*reinterpret_cast<uint32_t(*)[64]>(v), r, o);
+      scale_pack64(*reinterpret_cast<uint32_t(*)[64]>(v + 64), r, o + 32);
       if (row < T) store_row128<kV8>(out + row * (int64_t)N + c0, o);
     }
   }
