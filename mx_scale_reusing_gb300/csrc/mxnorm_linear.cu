@@ -29,16 +29,20 @@
 //                  contiguous), all completing on the leader's stage "full"
 //                  mbarrier (cta_group::2 form), which expects both CTAs'
 //                  bytes;
-//   warp 1 lane 0  leader CTA: MMA issuer.  Per stage it waits for
-//                  "sf_full", issues four tcgen05.mma and commits to the
+//   warp 1 lane 0  leader CTA: MMA issuer.  At every even stage it waits
+//                  for "sf_full" (which covers that stage and the next),
+//                  per stage it issues four tcgen05.mma and commits to the
 //                  "empty" mbarriers of both CTAs (multicast); after a tile's
 //                  last stage it commits to both CTAs' "acc_full";
-//   warp 2 lane 0  leader CTA: scale-factor copier.  Per stage it waits for
-//                  "full", copies the atoms into both CTAs' TMEM (tcgen05.cp,
-//                  cta_group::2: each CTA's shared memory into its own TMEM)
-//                  and commits to "sf_full".  Copies issued by the MMA thread
-//                  itself would wait between its stages; from a thread of
-//                  their own they overlap the MMAs in flight;
+//   warp 2 lane 0  leader CTA: scale-factor copier.  Per pair of stages
+//                  (2i, 2i + 1; the last alone when the count is odd) it
+//                  waits for each stage's "full", copies its atoms into both
+//                  CTAs' TMEM (tcgen05.cp, cta_group::2: each CTA's shared
+//                  memory into its own TMEM), then commits once to the even
+//                  stage's "sf_full".  Copies issued by the MMA thread itself
+//                  would wait between its stages; from a thread of their own
+//                  they overlap the MMAs in flight, and one hand-off per two
+//                  stages halves the issuer's waits;
 //   warps 3-10     epilogue (both CTAs), two per TMEM lane quadrant (32 rows)
 //                  with 128 columns each: tcgen05.ld of all 128 fp32
 //                  accumulators at once (one wait), then an arrival on the
@@ -349,8 +353,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         for (int kt = 0; kt < num_kt; ++kt, ++it) {
           const int s = (int)(it % kStages);
-          // the stage's operands have landed and its scale factors are in TMEM
-          if (!(ok = wait_bounded(sf_full0 + 8 * s, (uint32_t)(it / kStages) & 1u))) break;
+          // the stage's operands have landed and its scale factors are in TMEM: the copy warp
+          // signals once per pair of stages (2i, 2i + 1), on the even one's barrier
+          if (!(it & 1) && !(ok = wait_bounded(sf_full0 + 8 * s, (uint32_t)(it / kStages) & 1u))) break;
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
           const uint32_t tsf = tmem + 256 + 16 * s;
           const uint32_t a0 = saddr(sA + s * kStageA), b0 = saddr(sB + s * kStageB);
@@ -395,24 +400,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int64_t my_tiles = pair < tiles ? (tiles - 1 - pair) / npairs + 1 : 0;
       const int64_t total = my_tiles * num_kt;
       int sf_pos = 0, sf_buf = 0;  // the producer's scale-group walk, in step with it
-      for (int64_t it = 0; it < total; ++it) {
-        const int s = (int)(it % kStages);
-        if (!wait_bounded(full0 + 8 * s, (uint32_t)(it / kStages) & 1u)) break;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t tsf = tmem + 256 + 16 * s;
-        const uint32_t sf = saddr(sSF + sf_buf * sf_bytes) + (uint32_t)(sf_pos * 512);
-        if (++sf_pos == sf_group) {
-          sf_pos = 0;
-          if (++sf_buf == sf_bufs) sf_buf = 0;
+      bool ok = true;
+      for (int64_t it = 0; it < total && ok; it += 2) {
+        // a pair of stages (the last one alone when the count is odd), one signal
+        const int s0 = (int)(it % kStages);
+        for (int64_t jt = it; jt < it + 2 && jt < total; ++jt) {
+          const int s = (int)(jt % kStages);
+          if (!(ok = wait_bounded(full0 + 8 * s, (uint32_t)(jt / kStages) & 1u))) break;
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t tsf = tmem + 256 + 16 * s;
+          const uint32_t sf = saddr(sSF + sf_buf * sf_bytes) + (uint32_t)(sf_pos * 512);
+          if (++sf_pos == sf_group) {
+            sf_pos = 0;
+            if (++sf_buf == sf_bufs) sf_buf = 0;
+          }
+          asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf), "l"(desc_atom(sf)));
+          asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 4),
+                       "l"(desc_atom(sf + sf_group * 512)));
+          asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 8),
+                       "l"(desc_atom(sf + 2 * sf_group * 512)));
         }
-        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf), "l"(desc_atom(sf)));
-        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 4),
-                     "l"(desc_atom(sf + sf_group * 512)));
-        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tsf + 8),
-                     "l"(desc_atom(sf + 2 * sf_group * 512)));
+        if (!ok) break;
         asm volatile(
             "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                sf_full0 + 8 * s),
+                sf_full0 + 8 * s0),
             "h"((uint16_t)1)
             : "memory");
       }
