@@ -108,12 +108,18 @@ __device__ __forceinline__ unsigned long long gtimer() {
   return t;
 }
 
+// A waiting thread sleeps in try_wait until the phase completes or this
+// hint runs out, instead of spinning: the eight epilogue warps wait through
+// every tile's main loop, and spinning cost issue slots and power (8.7 %
+// slower at the power cap, 2 % in short bursts).
+constexpr uint32_t kSuspendHintNs = 1000000u;
+
 __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0u;
 }
