@@ -75,6 +75,9 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128;     // BM rows per CTA (256 per pair); BK bytes = E4M3 elements
 constexpr int kStages = 6;
+// The copy warp signals once per pair of stages (2i, 2i + 1) on the even
+// stage's barrier, so each barrier's uses stay kStages stages apart.
+static_assert(kStages % 2 == 0, "pairs of stages map onto the ring");
 constexpr int kStageA = BM * BK;                 // 16 KiB
 constexpr int kStageB = (BN / 2) * BK;           // 16 KiB: this CTA's half of the tile's w rows
 // Scale atoms (512 bytes: 128 rows x 4 blocks) of consecutive K stages are
