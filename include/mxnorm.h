@@ -58,8 +58,10 @@
  * baseline's first kernel, the gain-folded cast) are launched with
  * programmatic stream serialisation: each may be scheduled while the
  * previous kernel on the stream finishes, waits for that kernel's
- * completion before touching memory, and lets the next kernel be
- * scheduled early.  Stream order holds as usual; a kernel of the caller's
+ * completion before any load or store, and lets the next kernel be
+ * scheduled early.  Before the wait it may prefetch its first input rows
+ * into L2 (device memory only): a hint with no effect on what any load
+ * returns, since L2 is the GPU's point of coherence.  Stream order holds as usual; a kernel of the caller's
  * launched after one of them with the programmatic-serialisation attribute
  * must, as any programmatic dependent, wait (griddepcontrol.wait,
  * cudaGridDependencySynchronize) before reading its outputs.
