@@ -454,16 +454,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int64_t tile = pair; tile < tiles; tile += npairs, ++tcount) {
       if (!wait_bounded(acc_full, (uint32_t)(tcount & 1))) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      int64_t mt;
-      int nt;
-      tile_coords(tile, num_m, num_n, mt, nt);
-      const int64_t row = (2 * mt + rank) * BM + 32 * quad + lane;
-      const int c0 = nt * BN + 128 * half;
-      const float r = row < T ? inv_rms[row] : 0.0f;
-      const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(128 * half);
       // Read the warp's 32 x 128 share of the accumulators (all four loads
-      // in flight, one wait), then hand TMEM back to the MMA issuer before
-      // the row is converted and stored: the next tile's MMAs overlap both.
+      // in flight, one wait) and hand TMEM back to the MMA issuer first; the
+      // tile's coordinates and the row's inv_rms come after, off the MMAs'
+      // path, and the next tile's MMAs overlap the conversion and stores.
+      const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(128 * half);
       uint32_t v[128];
       tmem_load64(taddr, *reinterpret_cast<uint32_t(*)[64]>(v));
       tmem_load64(taddr + 64, *reinterpret_cast<uint32_t(*)[64]>(v + 64));
@@ -471,6 +466,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) arrive_remote(acc_empty_leader);
+      int64_t mt;
+      int nt;
+      tile_coords(tile, num_m, num_n, mt, nt);
+      const int64_t row = (2 * mt + rank) * BM + 32 * quad + lane;
+      const int c0 = nt * BN + 128 * half;
+      const float r = row < T ? inv_rms[row] : 0.0f;
       uint32_t o[64];
       scale_pack64(*reinterpret_cast<uint32_t(*)[64]>(v), r, o);
       scale_pack64(*reinterpret_cast<uint32_t(*)[64]>(v + 64), r, o + 32);
