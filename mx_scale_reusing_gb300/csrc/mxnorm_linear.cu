@@ -45,9 +45,10 @@
 //                  stages halves the issuer's waits;
 //   warps 3-10     epilogue (both CTAs), two per TMEM lane quadrant (32 rows)
 //                  with 128 columns each: tcgen05.ld of all 128 fp32
-//                  accumulators at once (one wait), then an arrival on the
-//                  leader's "acc_empty" (16 per tile) frees TMEM for the
-//                  next tile's MMAs; the values are multiplied by rho~[row],
+//                  accumulators at once (one wait), then, before any other
+//                  work, an arrival on the leader's "acc_empty" (16 per
+//                  tile) frees TMEM for the next tile's MMAs; the values are
+//                  multiplied by rho~[row],
 //                  rounded to packed bf16 in registers, and each lane stores
 //                  its row's 128 outputs straight to global memory (32-byte
 //                  stores when out is 32-byte aligned, else 16-byte ones).
@@ -114,7 +115,8 @@ __device__ __forceinline__ unsigned long long gtimer() {
 // A waiting thread sleeps in try_wait until the phase completes or this
 // hint runs out, instead of spinning: the eight epilogue warps wait through
 // every tile's main loop, and spinning cost issue slots and power (8.7 %
-// slower at the power cap, 2 % in short bursts).
+// slower at the power cap, about 3 % in short runs).  The single-thread
+// roles sleep too: letting them spin measured 11 % slower.
 constexpr uint32_t kSuspendHintNs = 1000000u;
 
 __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
